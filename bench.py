@@ -1,0 +1,439 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE expert-parallel dispatch / combine path on GB300.
+
+One step = one pass of the whole normal-mode path over one synthetic batch of
+the prefill workload (R=8 virtual ranks x T=4096 tokens, E=256, top-8,
+H=7168 bf16): layout -> notify (with its host sync) -> dispatch scatter ->
+permute -> combine, with the identity expert (expert_out = permuted_x).
+The same run also times the low-latency layer on the decode workload
+(R=16 x 128 tokens, FP8 send + receive/pack + BF16 combine) and reports it
+as ``ll_decode``.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine tokens/s and effective HBM GB/s (% of ~8 TB/s); LL µs/layer"
+L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes per launch from the ncu capture named in "source", for the
+# kernel bench.py reports as dominant (null until captured for this kernel).
+TRAFFIC = {}
+
+
+def measured_hbm_gbs():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes per unit of work (each row read or written once)
+# ---------------------------------------------------------------------------
+
+def algo_bytes(H, K, tokens, copies, pairs):
+    row = 2 * H
+    return {
+        "dispatch": (tokens + copies) * row,
+        "permute": (copies + pairs) * row,
+        "combine": (pairs + tokens) * row + tokens * K * 8,
+    }
+
+
+def ll_algo_bytes(H, tokens, pairs):
+    row = 2 * H
+    msg = H + H // 32 + 4
+    return {
+        "ll_send": tokens * row + pairs * msg,
+        "ll_recv": 2 * pairs * msg,
+        "ll_combine": pairs * row + tokens * row,
+    }
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (reported baseline; also the "reference" arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(workload, budget_s: float, min_s: float):
+    """Times the oracle's normal-mode chain on samples of the workload (T cut
+    down, same R, E, K, H, router) until min_s of CPU work has been done."""
+    import oracle
+    from combine_get_dispatch_histograms_gb300 import inputs
+    oracle.build()
+    T = 128 if workload.H >= 4096 else 1024
+    w = workload.replace(T=T)
+    tokens = 0
+    t_total = 0.0
+    seed = 100
+    while True:
+        x, idx, wts = inputs.make_inputs(w, seed=seed)
+        t = time.perf_counter()
+        oracle.run_normal(x, idx, wts, w.R, w.E, w.num_channels)
+        t_total += time.perf_counter() - t
+        tokens += w.R * w.T
+        seed += 1
+        if t_total >= min_s or t_total > budget_s:
+            break
+    return {"value": tokens / t_total, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{tokens} tokens: {seed - 100} batches of R={w.R} x T={w.T} (E={w.E}, K={w.K}, H={w.H}), "
+                      f"single-threaded plain C oracle, {t_total:.1f} s"}
+
+
+def run_reference(args, workload):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    steps = []
+    for _ in range(args.warmup):
+        oracle_sample(workload, budget_s=3.0, min_s=0.0)
+    for _ in range(args.steps):
+        r = oracle_sample(workload, budget_s=6.0, min_s=0.0)
+        steps.append(r)
+    value = statistics.median(s["value"] for s in steps)
+    cpu = dict(steps[-1])
+    cpu["value"] = value
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload.name, "R": workload.R, "E": workload.E, "K": workload.K,
+                   "T": workload.T, "H": workload.H},
+        "cpu_baseline": cpu,
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="prefill", choices=["prefill", "skewed", "hier"])
+    ap.add_argument("--tokens", type=int, default=0, help="override T (profiling on a smaller case)")
+    ap.add_argument("--no-ll", action="store_true", help="skip the low-latency decode leg")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+
+    from combine_get_dispatch_histograms_gb300 import inputs
+    workload = inputs.WORKLOADS[args.workload]
+    if args.tokens:
+        workload = workload.replace(T=args.tokens)
+    if args.impl == "reference":
+        return run_reference(args, workload)
+
+    import torch
+    from combine_get_dispatch_histograms_gb300 import Context, LLBuffer
+    from combine_get_dispatch_histograms_gb300 import dist as epdist
+
+    info = epdist.init_from_env("nccl")
+    world, rank, local = info.world, info.rank, info.local_rank
+    barrier, max_over_ranks, sum_over_ranks = epdist.barrier, epdist.max_over_ranks, epdist.sum_over_ranks
+
+    w = workload
+    R, E, K, T, H, C = w.R, w.E, w.K, w.T, w.H, w.num_channels
+    hier = w.num_nodes > 1
+    seed = epdist.rank_seed(0, rank)  # every rank processes its own batch (weak scaling)
+    topk_idx, topk_w = inputs.make_routing(w, seed)
+    x = inputs.make_x(w, seed, device="cuda")
+    idx_d, w_d = topk_idx.cuda(), topk_w.cuda()
+    ctx = Context(R, E, K, T, H, num_channels=C, num_nodes=w.num_nodes)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    # sizes from one notify, then buffers allocated once
+    lay = ctx.get_dispatch_layout(idx_d, nodes=hier)
+    handle = ctx.notify_dispatch(idx_d, lay)
+    recv = ctx.alloc_recv(handle.num_recv_rows)
+    perm = dict(permuted_x=torch.empty(handle.num_perm_rows, H, dtype=torch.bfloat16, device="cuda"),
+                perm_src_row=torch.empty(handle.num_perm_rows, dtype=torch.int32, device="cuda"))
+    out = torch.empty(R, T, H, dtype=torch.bfloat16, device="cuda")
+    staging = None
+    if hier:
+        S = handle.num_stage_rows
+        staging = dict(staging=torch.empty(S, H, dtype=torch.bfloat16, device="cuda"),
+                       stage_src_rank=torch.empty(S, dtype=torch.int32, device="cuda"),
+                       stage_src_idx=torch.empty(S, dtype=torch.int32, device="cuda"))
+    tokens = R * T
+    copies = handle.num_recv_rows
+    pairs = handle.num_perm_rows
+    names = ["layout", "notify", "dispatch", "permute", "combine"]
+    launches = {"layout": 1, "notify": 2, "dispatch": 2 if hier else 1, "permute": 1, "combine": 1}
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        ctx.get_dispatch_layout(idx_d, nodes=hier, out=lay)
+        mark(1)
+        ctx.notify_dispatch(idx_d, lay, handle=handle)
+        mark(2)
+        if hier:
+            ctx.dispatch_hier(x, idx_d, w_d, handle, out=recv, staging=staging)
+        else:
+            ctx.dispatch(x, idx_d, w_d, handle, out=recv)
+        mark(3)
+        ctx.permute(handle, recv, out=perm)
+        mark(4)
+        ctx.combine(handle, perm["permuted_x"], idx_d, w_d, out=out, hier=hier)
+        mark(5)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    ctx.check()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()  # L2 flush between steps, outside the step's events
+        step(evs[i])
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - wall0
+    ctx.check()
+    per = {n: [] for n in names}
+    step_ms = []
+    for ev in evs:
+        for j, n in enumerate(names):
+            per[n].append(ev[j].elapsed_time(ev[j + 1]))
+        step_ms.append(ev[0].elapsed_time(ev[5]))
+    local_ms = sum(step_ms) / len(step_ms)
+    ms = max_over_ranks(local_ms)
+    total_tokens = sum_over_ranks(tokens)
+    value = total_tokens / (ms / 1e3)
+
+    # ---- low-latency decode layer -------------------------------------------------
+    ll = None
+    if not args.no_ll:
+        dw = inputs.WORKLOADS["decode"]
+        d_idx, d_w = inputs.make_routing(dw, seed + 7)
+        d_x = inputs.make_x(dw, seed + 7, device="cuda")
+        d_idx_d, d_w_d = d_idx.cuda(), d_w.cuda()
+        buf = LLBuffer(dw.R, dw.E, dw.K, dw.T, dw.H, dw.ll_cap)
+        pk = buf.alloc_packed()
+        buf.dispatch(d_x, d_idx_d, out=pk)
+        # identity expert: y = bf16(code * scale) (outside the timed layer)
+        codes = pk["packed_x"].view(torch.float8_e4m3fn).float()
+        y_ll = (codes * pk["packed_scales"].repeat_interleave(128, dim=-1)).to(torch.bfloat16)
+        del codes
+        d_out = torch.empty(dw.R, dw.T, dw.H, dtype=torch.bfloat16, device="cuda")
+        for _ in range(args.warmup):
+            flush.zero_()
+            buf.dispatch(d_x, d_idx_d, out=pk)
+            buf.combine(y_ll, d_idx_d, d_w_d, pk, out=d_out)
+        buf.check()
+        lev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            lev[i][0].record(stream)
+            buf.send(d_x, d_idx_d, out=pk)
+            lev[i][1].record(stream)
+            buf.recv(pk)
+            lev[i][2].record(stream)
+            buf.combine(y_ll, d_idx_d, d_w_d, pk, out=d_out)
+            lev[i][3].record(stream)
+        torch.cuda.synchronize()
+        buf.check()
+        lname = ["ll_send", "ll_recv", "ll_combine"]
+        lper = {n: statistics.median(e[j].elapsed_time(e[j + 1]) for e in lev) for j, n in enumerate(lname)}
+        layer_us = statistics.median(e[0].elapsed_time(e[3]) for e in lev) * 1e3
+        d_pairs = int((d_idx >= 0).sum())
+        lbytes = ll_algo_bytes(dw.H, dw.R * dw.T, d_pairs)
+        peak, _ = measured_hbm_gbs()
+        ll = {"workload": "decode", "R": dw.R, "T": dw.T, "H": dw.H, "cap": dw.ll_cap,
+              "us_per_layer": round(layer_us, 2),
+              "kernels": {n: {"us": round(lper[n] * 1e3, 2), "algo_bytes": lbytes[n],
+                              "GBps": round(lbytes[n] / (lper[n] * 1e-3) / 1e9, 1),
+                              "frac": round(lbytes[n] / (lper[n] * 1e-3) / 1e9 / peak, 3)} for n in lname},
+              "l2": "flushed before each layer (512 MiB write), flush not timed"}
+        del y_ll, pk, buf
+
+    clocks = sampler.stop()
+
+    # ---- end to end through the public API with host buffers ------------------------
+    e2e = None
+    if not args.no_e2e:
+        x_h = x.cpu().pin_memory()
+        i_h = topk_idx.pin_memory()
+        w_h = topk_w.pin_memory()
+        out_h = torch.empty(R, T, H, dtype=torch.bfloat16).pin_memory()
+        x_dev = torch.empty_like(x)
+        i_dev = torch.empty_like(idx_d)
+        w_dev = torch.empty_like(w_d)
+
+        def e2e_step():
+            x_dev.copy_(x_h, non_blocking=True)
+            i_dev.copy_(i_h, non_blocking=True)
+            w_dev.copy_(w_h, non_blocking=True)
+            ctx.get_dispatch_layout(i_dev, nodes=hier, out=lay)
+            ctx.notify_dispatch(i_dev, lay, handle=handle)
+            if hier:
+                ctx.dispatch_hier(x_dev, i_dev, w_dev, handle, out=recv, staging=staging)
+            else:
+                ctx.dispatch(x_dev, i_dev, w_dev, handle, out=recv)
+            ctx.permute(handle, recv, out=perm)
+            ctx.combine(handle, perm["permuted_x"], i_dev, w_dev, out=out, hier=hier)
+            out_h.copy_(out, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            ee[i][0].record(stream)
+            e2e_step()
+            ee[i][1].record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in ee) / args.steps)
+        h2d = x.numel() * 2 + topk_idx.numel() * 8 + topk_w.numel() * 4
+        e2e = {"value": total_tokens / (e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": out.numel() * 2, "ms_per_step": round(e_ms, 4)}
+
+    if rank != 0:
+        epdist.shutdown()
+        return 0
+
+    # ---- roofline of the dominant kernel ------------------------------------------
+    peak, peak_kind = measured_hbm_gbs()
+    ab = algo_bytes(H, K, tokens, copies, pairs)
+    med = {n: statistics.median(per[n]) for n in names}
+    kernels = {}
+    for n in names:
+        entry = {"us": round(med[n] * 1e3, 2)}
+        if n in ab:
+            gbs = ab[n] / (med[n] * 1e-3) / 1e9
+            entry.update({"algo_bytes": ab[n], "GBps": round(gbs, 1), "frac": round(gbs / peak, 3)})
+        kernels[n] = entry
+    dom = max(ab, key=lambda n: med[n])
+    dom_avg_ms = sum(per[dom]) / len(per[dom])
+    achieved = ab[dom] / (dom_avg_ms * 1e-3) / 1e9
+    tr = TRAFFIC.get((w.name, dom))
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "algo_bytes_per_launch": ab[dom], "traffic": tr}
+
+    cpu = None
+    if not args.no_cpu and world >= 1:
+        cpu = oracle_sample(w, budget_s=25.0, min_s=10.0)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "R": R, "E": E, "K": K, "T": T, "H": H, "num_channels": C,
+                   "num_nodes": w.num_nodes, "router": w.router, "tokens_per_step_per_gpu": tokens,
+                   "copies": copies, "pairs": pairs,
+                   "l2": "flushed between steps (512 MiB write, not timed); every step's inputs exceed L2",
+                   "timing": "CUDA events on the launching stream, per step, mean over steps, max over ranks"},
+        "effective_GBps": round(sum(ab.values()) / (sum(med[n] for n in ab) * 1e-3) / 1e9, 1),
+        "kernels": kernels,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": sum(launches.values()) * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 4),
+        "ll_decode": ll,
+    }
+    print(json.dumps(line), flush=True)
+    epdist.shutdown()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

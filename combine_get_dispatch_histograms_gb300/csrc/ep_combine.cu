@@ -1,0 +1,232 @@
+// ep_combine.cu -- the weighted reductions back to the original token order:
+//
+//  * combine (page "DeepEP 学习笔记", sections "combine 过程" and "DeepEP v2 /
+//    direct 模式": the rank-level partial result of a token is reduced inside
+//    the rank that holds its experts, the epilogue reduces over destination
+//    ranks);
+//  * hierarchical combine (same page, section "hybrid 模式": local reduce inside
+//    the node, then the final reduce at the source);
+//  * low-latency BF16 combine (page "事件驱动 EP 内核的调度策略与零拷贝通信", section
+//    "低延迟模式": combine stays in BF16).
+//
+// One warp owns one token.  Lanes 0..K-1 read the token's top-k entries and
+// order them by (rank, k) (or by k for the low-latency mode); every lane then
+// owns 8 channels per step (one 16-byte vector per row), loads that vector
+// from each of the token's rows before accumulating (up to K 16-byte loads in
+// flight per lane), and reduces in fp32 with explicit fused multiply-adds in
+// the defined order.  The partial sums are never materialised: on one GPU a
+// "partial" is the grouping of the sum.  Output: bf16, round to nearest even.
+#include <climits>
+
+#include "ep_internal.cuh"
+#include "ep_combine.cuh"
+
+namespace ep {
+
+constexpr int kCombineThreads = 256;
+constexpr int kCombineWarps = kCombineThreads / 32;
+
+__device__ __forceinline__ void bf16x8_to_f32(const int4& v, float* f) {
+    const uint32_t u[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(u[i] << 16);
+        f[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ int4 f32x8_to_bf16(const float* f) {
+    uint32_t u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        u[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    return make_int4((int)u[0], (int)u[1], (int)u[2], (int)u[3]);
+}
+
+// MODE 0: flat (rank partials), 1: hierarchical (rank, node, final), 2: low-latency (k order)
+template <int KMAX, int MODE>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a) {
+    __shared__ int64_t sh_row[kCombineWarps][KMAX];
+    __shared__ float sh_w[kCombineWarps][KMAX];
+    __shared__ uint8_t sh_brk[kCombineWarps][KMAX];  // bit0: new rank group, bit1: new node group
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int K = a.K;
+    const int64_t n_tok = (int64_t)a.R * a.n;
+    const int nvec = a.H / 8;
+    const int64_t row_bytes = (int64_t)a.H * 2;
+    for (int64_t q = (int64_t)blockIdx.x * kCombineWarps + warp; q < n_tok; q += (int64_t)gridDim.x * kCombineWarps) {
+        const int s = (int)(q / a.n);
+        const int t = a.t0 + (int)(q % a.n);
+        const int64_t g = (int64_t)s * a.T + t;
+        // ---- entries of this token -------------------------------------------------
+        bool valid = false;
+        int d = INT_MAX;
+        int64_t row = 0;
+        float wk = 0.0f;
+        if (lane < K) {
+            const int64_t e = a.topk_idx[g * K + lane];
+            if (e >= 0 && e < a.E) {
+                d = (int)(e / a.L);
+                if (MODE == 2) {
+                    const int l = (int)(e % a.L);
+                    const int32_t sl = a.slot[g * K + lane];
+                    const int32_t begin = a.layout_range[(((int64_t)d * a.L + l) * a.R + s) * 2];
+                    row = ((int64_t)d * a.L + l) * a.rows_per_expert + begin + sl;
+                    valid = sl >= 0 && row >= 0 && row < a.y_rows;
+                } else {
+                    row = a.perm_pos[g * K + lane];
+                    valid = row >= 0 && row < a.y_rows;
+                }
+                if (!valid) flag(a.status, FLAG_BOUNDS);
+                wk = a.w[g * K + lane];
+            }
+        }
+        const int key = valid ? (MODE == 2 ? lane : d * 32 + lane) : INT_MAX;
+        int rank = 0;
+        bool new_rank = true, new_node = true;
+        for (int j = 0; j < K; ++j) {
+            const int kj = __shfl_sync(0xffffffffu, key, j);
+            const int dj = __shfl_sync(0xffffffffu, d, j);
+            if (kj < key) {
+                ++rank;
+                if (dj == d) new_rank = false;
+                if (dj / a.G == d / a.G) new_node = false;
+            }
+        }
+        const int nvalid = __popc(__ballot_sync(0xffffffffu, valid));
+        if (valid) {
+            sh_row[warp][rank] = row;
+            sh_w[warp][rank] = wk;
+            sh_brk[warp][rank] = (uint8_t)((new_rank ? 1 : 0) | (new_node ? 2 : 0));
+        }
+        __syncwarp();
+        int64_t roff[KMAX];
+        float wr[KMAX];
+        uint8_t br[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            roff[j] = j < nvalid ? sh_row[warp][j] * row_bytes : 0;
+            wr[j] = j < nvalid ? sh_w[warp][j] : 0.0f;
+            br[j] = j < nvalid ? sh_brk[warp][j] : 0;
+        }
+        __syncwarp();
+        const uint8_t* y = static_cast<const uint8_t*>(a.y);
+        int4* out = reinterpret_cast<int4*>(static_cast<uint8_t*>(a.out) + g * row_bytes);
+        // ---- channels ------------------------------------------------------------------
+        for (int c = lane; c < nvec; c += 32) {
+            int4 v[KMAX];
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                if (j < nvalid) v[j] = ld_nc_na_v4(y + roff[j] + (int64_t)c * 16);
+            float fin[8], nod[8], par[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) fin[i] = nod[i] = par[i] = 0.0f;
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                if (j < nvalid) {
+                    if (MODE != 2 && j > 0 && (br[j] & 1)) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            if (MODE == 1) {
+                                nod[i] = __fadd_rn(nod[i], par[i]);
+                                if (br[j] & 2) {
+                                    fin[i] = __fadd_rn(fin[i], nod[i]);
+                                    nod[i] = 0.0f;
+                                }
+                            } else {
+                                fin[i] = __fadd_rn(fin[i], par[i]);
+                            }
+                            par[i] = 0.0f;
+                        }
+                    }
+                    float yv[8];
+                    bf16x8_to_f32(v[j], yv);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) par[i] = __fmaf_rn(wr[j], yv[i], par[i]);
+                }
+            }
+            if (nvalid > 0) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (MODE == 1) {
+                        nod[i] = __fadd_rn(nod[i], par[i]);
+                        fin[i] = __fadd_rn(fin[i], nod[i]);
+                    } else if (MODE == 0) {
+                        fin[i] = __fadd_rn(fin[i], par[i]);
+                    } else {
+                        fin[i] = par[i];
+                    }
+                }
+            }
+            st_na_v4(out + c, f32x8_to_bf16(fin));
+        }
+    }
+}
+
+template <int MODE>
+static cudaError_t launch_mode(const CombineArgs& a, int grid, cudaStream_t s) {
+    if (a.K <= 8) combine_kernel<8, MODE><<<grid, kCombineThreads, 0, s>>>(a);
+    else if (a.K <= 16) combine_kernel<16, MODE><<<grid, kCombineThreads, 0, s>>>(a);
+    else combine_kernel<32, MODE><<<grid, kCombineThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+ep_status launch_combine(const CombineArgs& a, int mode, int num_sms, cudaStream_t s) {
+    const int64_t n_tok = (int64_t)a.R * a.n;
+    if (n_tok <= 0) return EP_OK;
+    int64_t want = (n_tok + kCombineWarps - 1) / kCombineWarps;
+    const int64_t cap = (int64_t)num_sms * 16;
+    const int grid = (int)(want < cap ? want : cap);
+    cudaError_t e = mode == 0 ? launch_mode<0>(a, grid, s) : mode == 1 ? launch_mode<1>(a, grid, s) : launch_mode<2>(a, grid, s);
+    if (e != cudaSuccess) return cuda_error(e, "combine kernel");
+    return EP_OK;
+}
+
+}  // namespace ep
+
+using namespace ep;
+
+static ep_status combine_common(ep_ctx* c, const ep_dispatch_handle* h, const void* y, int64_t perm_rows,
+                                const int64_t* topk_idx, const float* w, void* out, void* stream, int mode) {
+    if (!c || !h) return set_error(EP_ERR_INVALID_ARG, "ctx or handle is NULL");
+    c->last_launches = 0;
+    const ep_config& f = c->cfg;
+    if (f.num_tokens == 0) return EP_OK;
+    if (!out || !aligned16(out)) return set_error(EP_ERR_INVALID_ARG, "out must be a 16-byte aligned pointer");
+    if (perm_rows > 0 && (!y || !aligned16(y))) return set_error(EP_ERR_INVALID_ARG, "expert_out must be 16-byte aligned");
+    if (!topk_idx || !w || !h->perm_pos) return set_error(EP_ERR_INVALID_ARG, "NULL combine argument");
+    CombineArgs a{};
+    a.y = y;
+    a.y_rows = perm_rows;
+    a.topk_idx = topk_idx;
+    a.w = w;
+    a.perm_pos = h->perm_pos;
+    a.out = out;
+    a.R = f.num_ranks;
+    a.E = f.num_experts;
+    a.L = c->L;
+    a.K = f.num_topk;
+    a.T = f.num_tokens;
+    a.H = f.hidden;
+    a.G = mode == 1 ? c->G : f.num_ranks;
+    a.t0 = 0;
+    a.n = f.num_tokens;
+    a.status = c->status;
+    ep_status st = launch_combine(a, mode, c->num_sms, as_stream(stream));
+    if (st == EP_OK) c->last_launches = 1;
+    return st;
+}
+
+extern "C" ep_status ep_combine(ep_ctx* c, const ep_dispatch_handle* h, const void* expert_out, int64_t num_perm_rows,
+                                const int64_t* topk_idx, const float* topk_weights, void* out, void* stream) {
+    return combine_common(c, h, expert_out, num_perm_rows, topk_idx, topk_weights, out, stream, 0);
+}
+
+extern "C" ep_status ep_combine_hier(ep_ctx* c, const ep_dispatch_handle* h, const void* expert_out,
+                                     int64_t num_perm_rows, const int64_t* topk_idx, const float* topk_weights,
+                                     void* out, void* stream) {
+    if (c && c->cfg.num_nodes < 2) return set_error(EP_ERR_INVALID_ARG, "ep_combine_hier needs num_nodes > 1");
+    return combine_common(c, h, expert_out, num_perm_rows, topk_idx, topk_weights, out, stream, 1);
+}
