@@ -592,8 +592,11 @@ extern "C" ep_status ep_get_dispatch_layout(ep_ctx* c, const int64_t* topk_idx, 
     if (!c) return set_error(EP_ERR_INVALID_ARG, "ctx is NULL");
     c->last_launches = 0;
     const ep_config& f = c->cfg;
-    const bool nodes = ntpn != nullptr || itin != nullptr;
-    if (nodes && (!ntpn || !itin)) return set_error(EP_ERR_INVALID_ARG, "give both node outputs or neither");
+    // node outputs: num_tokens_per_node selects the hierarchical layout;
+    // is_token_in_node may be NULL only when there are no tokens
+    const bool nodes = ntpn != nullptr;
+    if (!nodes && itin) return set_error(EP_ERR_INVALID_ARG, "is_token_in_node given without num_tokens_per_node");
+    if (nodes && !itin && f.num_tokens > 0) return set_error(EP_ERR_INVALID_ARG, "is_token_in_node is NULL");
     if (!ntpe || !ntpr || (!itir && f.num_tokens > 0) || (!topk_idx && f.num_tokens > 0))
         return set_error(EP_ERR_INVALID_ARG, "NULL layout pointer");
     const int N = nodes ? f.num_nodes : 0;
@@ -618,7 +621,7 @@ extern "C" ep_status ep_notify_dispatch(ep_ctx* c, const int64_t* topk_idx, cons
     const bool hier = f.num_nodes > 1;
     if (!ntpe || !ntpr || !host_num_recv || (f.num_tokens > 0 && (!itir || !topk_idx)))
         return set_error(EP_ERR_INVALID_ARG, "NULL notify input");
-    if (hier && (!ntpn || (!itin && f.num_tokens > 0) || !h->stage_base || !h->stage_pos))
+    if (hier && (!ntpn || !h->stage_base || (f.num_tokens > 0 && (!itin || !h->stage_pos))))
         return set_error(EP_ERR_INVALID_ARG, "hierarchical mode needs node layout and stage_* handle arrays");
     if (!h->recv_count || !h->recv_offsets || !h->num_recv_tokens || !h->rank_base || !h->num_recv_per_expert ||
         !h->expert_offsets || !h->perm_rank_base || !h->channel_prefix_matrix ||
