@@ -18,6 +18,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "ep_internal.cuh"
@@ -607,6 +608,66 @@ extern "C" ep_status ep_get_dispatch_layout(ep_ctx* c, const int64_t* topk_idx, 
         itir, ntpn, itin, c->ws_layout_part, c->ws_layout_done, c->status);
     EP_CHECK_LAUNCH("layout_kernel");
     c->last_launches = 1;
+    return EP_OK;
+}
+
+// ============================================================================
+// Allocation-free layout (see ep.h): the same layout kernel, with its scratch
+// in a fixed device array of this library instead of a context's workspace.
+// ============================================================================
+namespace {
+constexpr size_t kNoAllocScratchInts = EP_LAYOUT_NOALLOC_SCRATCH_BYTES / sizeof(int32_t);
+constexpr size_t kNoAllocHeaderInts = 128;  // [0, 64) completion counters, [64] status
+constexpr int kNoAllocMaxDevices = 64;
+static __device__ __align__(256) int32_t g_noalloc_layout_scratch[kNoAllocScratchInts];
+std::mutex g_noalloc_mu;
+int32_t* g_noalloc_scratch_dev[kNoAllocMaxDevices];  // device address of the array, per device
+}  // namespace
+
+extern "C" ep_status ep_get_dispatch_layout_noalloc(int32_t R, int32_t E, int32_t K, int32_t T, int32_t num_nodes,
+                                                    const int64_t* topk_idx, int32_t* ntpe, int32_t* ntpr,
+                                                    uint8_t* itir, int32_t* ntpn, uint8_t* itin,
+                                                    uint32_t* status_out, void* stream) {
+    if (R < 1 || R > kMaxRanks || E < 1 || E > kMaxExperts || E % R || E / R > kMaxLocalExperts || K < 1 ||
+        K > kMaxTopk || T < 0 || num_nodes < 1 || num_nodes > R || R % num_nodes)
+        return set_error(EP_ERR_INVALID_ARG, "bad sizes (R %d, E %d, K %d, T %d, nodes %d)", R, E, K, T, num_nodes);
+    if ((int64_t)R * T * (K > R ? K : R) >= (1ll << 31)) return set_error(EP_ERR_INVALID_ARG, "R*T*max(K,R) >= 2^31");
+    const bool nodes = ntpn != nullptr;
+    if (!nodes && itin) return set_error(EP_ERR_INVALID_ARG, "is_token_in_node given without num_tokens_per_node");
+    if (!ntpe || !ntpr || (T > 0 && (!itir || !topk_idx || (nodes && !itin))))
+        return set_error(EP_ERR_INVALID_ARG, "NULL layout pointer");
+    const int N = nodes ? num_nodes : 0;
+    const TileGeom geom = make_tiles(T, 1);
+    const int W = E + R + N;
+    const size_t need = kNoAllocHeaderInts + (size_t)R * geom.tiles_per_src * W;
+    if (need > kNoAllocScratchInts)
+        return set_error(EP_ERR_CAPACITY,
+                         "the allocation-free layout needs %zu bytes of scratch, it has %u; use ep_get_dispatch_layout",
+                         need * sizeof(int32_t), (unsigned)EP_LAYOUT_NOALLOC_SCRATCH_BYTES);
+    int dev = 0;
+    EP_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return set_error(EP_ERR_INVALID_ARG, "device index %d not supported", dev);
+    int32_t* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (!g_noalloc_scratch_dev[dev]) {
+            void* p = nullptr;
+            cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_layout_scratch);
+            if (e != cudaSuccess) return cuda_error(e, "cudaGetSymbolAddress(layout scratch)");
+            g_noalloc_scratch_dev[dev] = static_cast<int32_t*>(p);
+        }
+        scratch = g_noalloc_scratch_dev[dev];
+    }
+    cudaStream_t s = as_stream(stream);
+    // completion counters and the status word must start at zero
+    EP_CUDA(cudaMemsetAsync(scratch, 0, kNoAllocHeaderInts * sizeof(int32_t), s));
+    uint32_t* done = reinterpret_cast<uint32_t*>(scratch);
+    uint32_t* status = status_out ? status_out : reinterpret_cast<uint32_t*>(scratch + 64);
+    dim3 grid(geom.tiles_per_src, R);
+    layout_kernel<<<grid, kTileTokens, sizeof(int32_t) * W, s>>>(topk_idx, R, E, K, T, E / R, N, R / num_nodes, geom,
+                                                                 ntpe, ntpr, itir, ntpn, itin,
+                                                                 scratch + kNoAllocHeaderInts, done, status);
+    EP_CHECK_LAUNCH("layout_kernel (allocation-free)");
     return EP_OK;
 }
 

@@ -114,6 +114,41 @@ ep_status ep_get_dispatch_layout(ep_ctx* ctx, const int64_t* topk_idx,
                                  uint8_t* is_token_in_rank, int32_t* num_tokens_per_node,
                                  uint8_t* is_token_in_node, void* stream);
 
+/* Allocation-free layout.  The pages have no counterpart of this entry point;
+ * it exists for callers that must not allocate device memory themselves: for
+ * example a plug-in inside a serving runtime that owns every byte of HBM
+ * through its own pool and hands out only the tensors it manages, or a
+ * latency-critical path where cudaMalloc / cudaFree (which can synchronise
+ * the whole device and can fail once the memory is reserved) are not allowed.
+ * It computes exactly what ep_get_dispatch_layout computes, without a context:
+ * its scratch (per-tile partial counts, per-source completion counters, a
+ * status word) is a fixed array in the library's device memory of
+ * EP_LAYOUT_NOALLOC_SCRATCH_BYTES, held by every GPU that loads the library
+ * until the process exits.  It calls no allocating routine.
+ *   - Sizes: num_ranks 1..64, num_experts a multiple of num_ranks and <= 4096,
+ *     num_topk 1..32, num_tokens >= 0, num_nodes 1..num_ranks dividing
+ *     num_ranks (node outputs are written only when num_tokens_per_node is
+ *     non-NULL).  The scratch needed is
+ *     4 * (128 + R * ceil(max(T,1) / 256) * (E + R + N)) bytes, N = num_nodes
+ *     when node outputs are requested and 0 otherwise; a call that
+ *     needs more than EP_LAYOUT_NOALLOC_SCRATCH_BYTES returns EP_ERR_CAPACITY
+ *     and launches nothing (use ep_get_dispatch_layout instead).
+ *   - status_out (device, nullable): if given, the kernel ORs its error bits
+ *     into it (1 = a topk_idx value outside [-1, E) was skipped); the caller
+ *     zeroes it.
+ *   - The first call on a device looks up the scratch array's device address
+ *     (once per device, with that device current); make that first call before
+ *     any stream capture.  Every call clears the counters it needs before its
+ *     kernel runs, on `stream`.  All calls share the one array: calls whose
+ *     kernels overlap on the GPU (other streams, other threads) race and give
+ *     wrong results; order them on one stream. */
+#define EP_LAYOUT_NOALLOC_SCRATCH_BYTES (1u << 20)
+ep_status ep_get_dispatch_layout_noalloc(int32_t num_ranks, int32_t num_experts, int32_t num_topk,
+                                         int32_t num_tokens, int32_t num_nodes, const int64_t* topk_idx,
+                                         int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                                         uint8_t* is_token_in_rank, int32_t* num_tokens_per_node,
+                                         uint8_t* is_token_in_node, uint32_t* status_out, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Notify: count exchange, ragged offsets, channel prefix, positions          */
 /* ([P1] 事件驱动调度的本质 / 高吞吐量模式; [P2] notify_dispatch steps 1-3)        */

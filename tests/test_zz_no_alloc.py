@@ -1,0 +1,71 @@
+"""The allocation-free layout entry point, called through the C ABI, against
+the context-based ep_get_dispatch_layout on the same inputs, twice in a row.
+
+This entry point serves callers that may not allocate device memory
+themselves (for example a plug-in whose host runtime owns all of HBM through
+its own pool): it keeps its scratch in a fixed array inside the library.
+The file is named so that pytest collects it last."""
+import ctypes
+
+import pytest
+import torch
+
+from combine_get_dispatch_histograms_gb300 import Context, _lib, inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _noalloc(lib, R, E, K, T, N, idx, with_nodes):
+    dev = idx.device
+    o = dict(
+        num_tokens_per_expert=torch.full((R, E), -7, dtype=torch.int32, device=dev),
+        num_tokens_per_rank=torch.full((R, R), -7, dtype=torch.int32, device=dev),
+        is_token_in_rank=torch.full((R, T, R), 9, dtype=torch.uint8, device=dev),
+    )
+    if with_nodes:
+        o["num_tokens_per_node"] = torch.full((R, N), -7, dtype=torch.int32, device=dev)
+        o["is_token_in_node"] = torch.full((R, T, N), 9, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = lib.ep_get_dispatch_layout_noalloc(
+        R, E, K, T, N, _p(idx), _p(o["num_tokens_per_expert"]), _p(o["num_tokens_per_rank"]),
+        _p(o["is_token_in_rank"]), _p(o.get("num_tokens_per_node")), _p(o.get("is_token_in_node")),
+        _p(status), stream)
+    assert rc == 0, lib.ep_last_error()
+    torch.cuda.synchronize()
+    return o, int(status.item())
+
+
+@pytest.mark.parametrize("R,E,K,T,N,mask_p,seed", [
+    (4, 8, 2, 16, 1, 0.0, 0),        # the tiny worked shape
+    (8, 256, 8, 4096, 1, 0.0, 1),    # the prefill routing
+    (32, 256, 8, 700, 4, 0.05, 2),   # nodes, masks, ragged last tile
+    (4, 8, 2, 0, 2, 0.0, 3),         # no tokens
+])
+def test_noalloc_layout_equals_context_layout_twice(R, E, K, T, N, mask_p, seed):
+    lib = _lib.load()
+    idx = inputs.random_topk(R, E, K, T, seed, mask_p).cuda()
+    with_nodes = N > 1
+    ctx = Context(R, E, K, T, 64, num_channels=8, num_nodes=N)
+    ref = ctx.get_dispatch_layout(idx, nodes=with_nodes)
+    torch.cuda.synchronize()
+    for call in range(2):
+        got, status = _noalloc(lib, R, E, K, T, N, idx, with_nodes)
+        assert status == 0
+        for k, v in ref.items():
+            assert torch.equal(got[k], v), (call, k)
+
+
+def test_noalloc_rejects_oversized_problems():
+    lib = _lib.load()
+    R, E, K, T = 64, 4096, 8, 10000  # needs about 40 MB of scratch
+    idx = torch.zeros(1, dtype=torch.int64, device="cuda")
+    dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
+    rc = lib.ep_get_dispatch_layout_noalloc(R, E, K, T, 1, _p(idx), _p(dummy), _p(dummy), _p(dummy), None, None,
+                                            None, None)
+    assert rc == -3
+    assert b"scratch" in lib.ep_last_error()
