@@ -56,9 +56,16 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
     const int64_t n_tok = (int64_t)a.R * a.n;
     const int nvec = a.H / 8;
     const int64_t row_bytes = (int64_t)a.H * 2;
-    for (int64_t q = (int64_t)blockIdx.x * kCombineWarps + warp; q < n_tok; q += (int64_t)gridDim.x * kCombineWarps) {
-        const int s = (int)(q / a.n);
-        const int t = a.t0 + (int)(q % a.n);
+    // a work item is (token, channel slice); small batches use several slices
+    // per token so that enough loads are in flight
+    const int per = (nvec + a.splits - 1) / a.splits;
+    const int64_t n_items = n_tok * a.splits;
+    for (int64_t q = (int64_t)blockIdx.x * kCombineWarps + warp; q < n_items; q += (int64_t)gridDim.x * kCombineWarps) {
+        const int64_t tok = q / a.splits;
+        const int c_lo = (int)(q % a.splits) * per;
+        const int c_hi = min(nvec, c_lo + per);
+        const int s = (int)(tok / a.n);
+        const int t = a.t0 + (int)(tok % a.n);
         const int64_t g = (int64_t)s * a.T + t;
         // ---- entries of this token -------------------------------------------------
         bool valid = false;
@@ -115,7 +122,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
         const uint8_t* y = static_cast<const uint8_t*>(a.y);
         int4* out = reinterpret_cast<int4*>(static_cast<uint8_t*>(a.out) + g * row_bytes);
         // ---- channels ------------------------------------------------------------------
-        for (int c = lane; c < nvec; c += 32) {
+        for (int c = c_lo + lane; c < c_hi; c += 32) {
             int4 v[KMAX];
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
@@ -176,10 +183,21 @@ static cudaError_t launch_mode(const CombineArgs& a, int grid, cudaStream_t s) {
 ep_status launch_combine(const CombineArgs& a, int mode, int num_sms, cudaStream_t s) {
     const int64_t n_tok = (int64_t)a.R * a.n;
     if (n_tok <= 0) return EP_OK;
-    int64_t want = (n_tok + kCombineWarps - 1) / kCombineWarps;
+    CombineArgs b = a;
+    // channel slices per token: aim for about 48 warps per SM, at least one
+    // 16-byte vector per lane per slice
+    const int nvec = a.H / 8;
+    const int64_t target = (int64_t)num_sms * 48;
+    int splits = (int)((target + n_tok - 1) / n_tok);
+    if (splits > nvec / 32) splits = nvec / 32;
+    if (splits > 8) splits = 8;
+    if (splits < 1) splits = 1;
+    b.splits = splits;
+    const int64_t items = n_tok * splits;
+    int64_t want = (items + kCombineWarps - 1) / kCombineWarps;
     const int64_t cap = (int64_t)num_sms * 16;
     const int grid = (int)(want < cap ? want : cap);
-    cudaError_t e = mode == 0 ? launch_mode<0>(a, grid, s) : mode == 1 ? launch_mode<1>(a, grid, s) : launch_mode<2>(a, grid, s);
+    cudaError_t e = mode == 0 ? launch_mode<0>(b, grid, s) : mode == 1 ? launch_mode<1>(b, grid, s) : launch_mode<2>(b, grid, s);
     if (e != cudaSuccess) return cuda_error(e, "combine kernel");
     return EP_OK;
 }

@@ -17,6 +17,7 @@ struct CombineArgs {
     void* out;                // bf16 [R][T][H]
     int R, E, L, K, T, H, G;
     int t0, n;                // tokens [t0, t0 + n) of every source rank
+    int splits;               // channel slices per token (set by launch_combine)
     uint32_t* status;
 };
 

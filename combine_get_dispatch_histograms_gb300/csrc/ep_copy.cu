@@ -28,7 +28,6 @@ namespace ep {
 constexpr int kCopyThreads = 128;
 constexpr int kBuilderThreads = kCopyThreads - 32;
 constexpr int kBatch = 32;      // units per table batch
-constexpr int kMaxFanout = 64;  // destinations per unit
 constexpr int kMaxStages = 16;
 
 struct CopyGeom {
@@ -211,7 +210,7 @@ __device__ void build_batch(const Route& route, const CopyGeom& g, const EngineS
     }
 }
 
-template <class Route>
+template <class Route, int DEPTH>
 __global__ void __launch_bounds__(kCopyThreads) copy_engine_kernel(Route route, CopyGeom g) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     EngineSmem sm;
@@ -278,9 +277,10 @@ __global__ void __launch_bounds__(kCopyThreads) copy_engine_kernel(Route route, 
                 for (int q = 0; q < n; ++q)
                     bulk_s2g(route.dst(rows[(size_t)i * g.fanout + q]) + (int64_t)c * g.chunk_bytes, sbuf, bytes);
                 bulk_commit();
-                // the group of job j-1 has finished reading its stage: refill it
-                bulk_wait_read<1>();
-                if (j >= 1 && issued < J) {
+                // the groups up to job j-DEPTH have finished reading their stages:
+                // refill the stage of job j-DEPTH
+                bulk_wait_read<DEPTH>();
+                if (j >= DEPTH && issued < J) {
                     issue_load(issued);
                     ++issued;
                 }
@@ -306,6 +306,7 @@ __global__ void __launch_bounds__(kCopyThreads) copy_engine_kernel(Route route, 
 struct EngineLaunch {
     CopyGeom g;
     int grid;
+    int depth;  // bulk store groups allowed to be reading shared memory
     size_t smem;
 };
 
@@ -316,8 +317,9 @@ static EngineLaunch plan_engine(const ep_ctx* c, int64_t n_units, int64_t row_by
     p.g.fanout = fanout;
     p.g.timeout_ns = c->wait_timeout_ns;
     p.g.status = c->status;
-    // two CTAs per SM, each with about 100 KB of staging
-    const size_t budget = 100 * 1024;
+    p.depth = c->copy_read_depth;
+    // copy_ctas_per_sm persistent CTAs per SM, each with copy_stage_bytes of staging
+    const size_t budget = (size_t)c->copy_stage_bytes;
     const size_t fixed = engine_stage_offset(fanout);
     const size_t stage_room = budget > fixed ? budget - fixed : 16 * 1024;
     int64_t chunk = row_bytes;
@@ -327,29 +329,35 @@ static EngineLaunch plan_engine(const ep_ctx* c, int64_t n_units, int64_t row_by
     p.g.nchunks = (int32_t)((row_bytes + chunk - 1) / chunk);
     int stages = (int)(stage_room / (size_t)chunk);
     if (stages > kMaxStages) stages = kMaxStages;
-    if (stages < 2) stages = 2;
+    if (stages < p.depth + 1) stages = p.depth + 1;
     p.g.stages = stages;
     p.smem = fixed + (size_t)stages * chunk;
-    const int64_t max_grid = (int64_t)c->num_sms * 2;
+    const int64_t max_grid = (int64_t)c->num_sms * c->copy_ctas_per_sm;
     const int64_t want = (n_units + 7) / 8;  // at least 8 units per CTA
     p.grid = (int)(want < max_grid ? (want < 1 ? 1 : want) : max_grid);
     return p;
 }
 
+template <class Route, int DEPTH>
+static ep_status launch_depth(const Route& r, const EngineLaunch& p, cudaStream_t s, const char* what) {
+    cudaError_t e = cudaFuncSetAttribute(copy_engine_kernel<Route, DEPTH>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+    if (e != cudaSuccess) return cuda_error(e, what);
+    copy_engine_kernel<Route, DEPTH><<<p.grid, kCopyThreads, p.smem, s>>>(r, p.g);
+    EP_CHECK_LAUNCH(what);
+    return EP_OK;
+}
+
 template <class Route>
 static ep_status launch_engine(const ep_ctx* c, const Route& r, const EngineLaunch& p, cudaStream_t s,
                                const char* what) {
+    (void)c;
     if (p.g.n_units <= 0) return EP_OK;
-    static bool configured = false;  // per template instance
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(copy_engine_kernel<Route>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             200 * 1024);
-        if (e != cudaSuccess) return cuda_error(e, what);
-        configured = true;
+    switch (p.depth) {
+        case 1: return launch_depth<Route, 1>(r, p, s, what);
+        case 2: return launch_depth<Route, 2>(r, p, s, what);
+        default: return launch_depth<Route, 3>(r, p, s, what);
     }
-    copy_engine_kernel<Route><<<p.grid, kCopyThreads, p.smem, s>>>(r, p.g);
-    EP_CHECK_LAUNCH(what);
-    return EP_OK;
 }
 
 }  // namespace ep

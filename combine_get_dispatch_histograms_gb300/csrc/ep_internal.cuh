@@ -94,6 +94,9 @@ struct ep_ctx {
     int32_t* host_block_dev;
     cudaEvent_t ev_counts;
     int64_t wait_timeout_ns;
+    // copy-engine launch shape (defaults; EP_COPY_CTAS_PER_SM, EP_COPY_STAGE_KB and
+    // EP_COPY_READ_DEPTH override them at context creation)
+    int copy_ctas_per_sm, copy_stage_bytes, copy_read_depth;
     // totals of the last notify (host copies), sizes of later launches
     int64_t last_total_recv, last_total_perm, last_total_stage;
     int last_launches;

@@ -17,6 +17,7 @@
 // the original design is stream order.
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -492,6 +493,13 @@ static ep_status validate_config(const ep_config* c) {
     return EP_OK;
 }
 
+static int env_int(const char* name, int dflt, int lo, int hi) {
+    const char* v = getenv(name);
+    if (!v || !*v) return dflt;
+    int x = atoi(v);
+    return x < lo ? lo : (x > hi ? hi : x);
+}
+
 static size_t notify_position_smem(const ep_ctx* c) {
     const int R = c->cfg.num_ranks, E = c->cfg.num_experts, N = c->cfg.num_nodes > 1 ? c->cfg.num_nodes : 0;
     return sizeof(int32_t) * (size_t)(E + R + N + R + kWarps * E + kWarps * (R + N));
@@ -509,6 +517,9 @@ extern "C" ep_status ep_ctx_create(const ep_config* cfg, ep_ctx** out) {
     c->G = cfg->num_ranks / cfg->num_nodes;
     c->tiles = make_tiles(cfg->num_tokens, cfg->num_channels);
     c->wait_timeout_ns = 2000000000ll;
+    c->copy_ctas_per_sm = env_int("EP_COPY_CTAS_PER_SM", 2, 1, 8);
+    c->copy_stage_bytes = env_int("EP_COPY_STAGE_KB", 64, 16, 220) * 1024;
+    c->copy_read_depth = env_int("EP_COPY_READ_DEPTH", 2, 1, 3);
     cudaError_t e = cudaGetDevice(&c->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
     if (e != cudaSuccess) {

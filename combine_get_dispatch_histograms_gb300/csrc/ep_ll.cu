@@ -41,7 +41,7 @@ struct ep_ll_buffer {
 
 namespace ep {
 
-constexpr int kSendThreads = 256;
+constexpr int kSendThreads = 1024;
 constexpr int kRecvThreads = 128;
 
 struct LLSendArgs {
@@ -62,130 +62,149 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
     return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
-__global__ void __launch_bounds__(kSendThreads) ll_send_kernel(LLSendArgs a) {
-    extern __shared__ int32_t sh_hist[];  // [E] (last CTA of a source)
+// grid = (n tokens, R sources), one CTA per token.  All loads of the CTA (its
+// own top-k entries, the source's earlier entries of the microbatch, the x row)
+// are issued before the first barrier; the slots come from shared-memory
+// counts; the token is quantised once and stored to its K regions.  No fence
+// or atomic on global memory: the counts are published by ll_publish_kernel.
+constexpr int kPriorPerThread = 8;
+
+__global__ void __launch_bounds__(1024) ll_send_kernel(LLSendArgs a) {
     __shared__ int sh_e[kMaxTopk];
     __shared__ int sh_cnt[kMaxTopk];
     __shared__ int sh_slot[kMaxTopk];
-    __shared__ bool is_last;
     const int s = blockIdx.y, j = blockIdx.x;  // j-th token of the microbatch
     const int K = a.K, R = a.R, E = a.E, H = a.H;
-    const int lane = threadIdx.x & 31;
-    // reset the other ping-pong buffer's count slots of this source
-    if (j == 0)
-        for (int e = threadIdx.x; e < E; e += blockDim.x) st_relaxed_gpu(a.other_counts + (int64_t)e * R + s, -1);
-
-    if (j < a.n) {
-        const int t = a.t0 + j;
-        const int64_t g = (int64_t)s * a.T + t;
-        if (threadIdx.x < K) {
-            const int64_t e = a.topk_idx[g * K + threadIdx.x];
-            int ev = -1;
-            if (e >= 0 && e < E) ev = (int)e;
-            else if (e != -1) flag(a.status, FLAG_INVALID_TOPK);
-            sh_e[threadIdx.x] = ev;
-            sh_cnt[threadIdx.x] = 0;
-        }
-        __syncthreads();
-        // slot = #earlier entries of this source in the microbatch with the same expert
-        const int64_t* first = a.topk_idx + ((int64_t)s * a.T + a.t0) * K;
-        const int prior = j * K;
-        for (int i = threadIdx.x; i < prior; i += blockDim.x) {
-            const int64_t e = first[i];
-            if (e < 0) continue;
+    // let the publish kernel start its own (independent) work early
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int t = a.t0 + j;
+    const int64_t g = (int64_t)s * a.T + t;
+    const int64_t* first = a.topk_idx + ((int64_t)s * a.T + a.t0) * K;
+    const int prior = j * K;
+    // ---- loads ---------------------------------------------------------------------
+    if (threadIdx.x < K) {
+        const int64_t e = a.topk_idx[g * K + threadIdx.x];
+        int ev = -1;
+        if (e >= 0 && e < E) ev = (int)e;
+        else if (e != -1) flag(a.status, FLAG_INVALID_TOPK);
+        sh_e[threadIdx.x] = ev;
+        sh_cnt[threadIdx.x] = 0;
+    }
+    int pe[kPriorPerThread];
+#pragma unroll
+    for (int u = 0; u < kPriorPerThread; ++u) {
+        const int i = threadIdx.x + u * blockDim.x;
+        const int64_t e = i < prior ? first[i] : -1;
+        pe[u] = (e >= 0 && e < E) ? (int)e : -1;
+    }
+    const int ngroups = H / 16;  // 16 channels per thread per pass; 8 groups per scale block
+    const uint16_t* xr = a.x + g * H;
+    int4 p0 = make_int4(0, 0, 0, 0), p1 = make_int4(0, 0, 0, 0);
+    if ((int)threadIdx.x < ngroups) {
+        p0 = ld_nc_na_v4(xr + threadIdx.x * 16);
+        p1 = ld_nc_na_v4(xr + threadIdx.x * 16 + 8);
+    }
+    __syncthreads();
+    // ---- slots: earlier entries of this source with the same expert ----------------
+#pragma unroll
+    for (int u = 0; u < kPriorPerThread; ++u)
+        if (pe[u] >= 0)
             for (int k = 0; k < K; ++k)
-                if (sh_e[k] == (int)e) atomicAdd(&sh_cnt[k], 1);
-        }
-        __syncthreads();
-        if (threadIdx.x < K) {
-            const int k = threadIdx.x;
-            const int ev = sh_e[k];
-            int sl = -1;
-            if (ev >= 0) {
-                sl = sh_cnt[k];
-                for (int k2 = 0; k2 < k; ++k2) sl += (sh_e[k2] == ev);
-                if (sl >= a.cap) {
-                    flag(a.status, FLAG_CAPACITY);
-                    sl = -1;
-                }
-            }
-            sh_slot[k] = sl;
-            a.slot_out[g * K + k] = ev >= 0 ? (sl >= 0 ? sl : -1) : -1;
-        }
-        __syncthreads();
-        // quantise once, store to every destination region
-        const int ngroups = H / 16;  // 16 channels per thread per pass; 8 groups per scale block
-        const uint16_t* xr = a.x + g * H;
-        for (int gi0 = 0; gi0 < ngroups; gi0 += blockDim.x) {
-            const int gi = gi0 + threadIdx.x;
-            const bool act = gi < ngroups;
-            float v[16];
-            float amax = 0.0f;
-            if (act) {
-                const int4 p0 = ld_nc_na_v4(xr + gi * 16);
-                const int4 p1 = ld_nc_na_v4(xr + gi * 16 + 8);
-                const uint32_t u[8] = {(uint32_t)p0.x, (uint32_t)p0.y, (uint32_t)p0.z, (uint32_t)p0.w,
-                                       (uint32_t)p1.x, (uint32_t)p1.y, (uint32_t)p1.z, (uint32_t)p1.w};
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    v[2 * i] = __uint_as_float(u[i] << 16);
-                    v[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
-                }
-#pragma unroll
-                for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = 0.0f;
-            }
-            // max over the 8 lanes holding one 128-channel block
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const float scale = __fdiv_rn(amax, 448.0f);
-            uint32_t w4[4];
-            if (scale == 0.0f) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    uint32_t c = 0;
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) c |= ((__float_as_uint(v[4 * i + b]) >> 31) ? 0x80u : 0u) << (8 * b);
-                    w4[i] = c;
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t lo = e4m3x2(__fdiv_rn(v[4 * i], scale), __fdiv_rn(v[4 * i + 1], scale));
-                    const uint32_t hi = e4m3x2(__fdiv_rn(v[4 * i + 2], scale), __fdiv_rn(v[4 * i + 3], scale));
-                    w4[i] = (lo & 0xffffu) | (hi << 16);
-                }
-            }
-            if (act) {
-                const int4 codes = make_int4((int)w4[0], (int)w4[1], (int)w4[2], (int)w4[3]);
-                for (int k = 0; k < K; ++k) {
-                    const int sl = sh_slot[k];
-                    if (sl < 0) continue;
-                    uint8_t* msg = a.regions + (((int64_t)sh_e[k] * R + s) * a.cap + sl) * a.msg_bytes;
-                    st_na_v4(msg + 16 + (int64_t)gi * 16, codes);
-                    if ((gi & 7) == 0) *reinterpret_cast<float*>(msg + 16 + H + (gi >> 3) * 4) = scale;
-                }
+                if (sh_e[k] == pe[u]) atomicAdd(&sh_cnt[k], 1);
+    for (int i = threadIdx.x + kPriorPerThread * blockDim.x; i < prior; i += blockDim.x) {
+        const int64_t e = first[i];
+        if (e < 0 || e >= E) continue;
+        for (int k = 0; k < K; ++k)
+            if (sh_e[k] == (int)e) atomicAdd(&sh_cnt[k], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < K) {
+        const int k = threadIdx.x;
+        const int ev = sh_e[k];
+        int sl = -1;
+        if (ev >= 0) {
+            sl = sh_cnt[k];
+            for (int k2 = 0; k2 < k; ++k2) sl += (sh_e[k2] == ev);
+            if (sl >= a.cap) {
+                flag(a.status, FLAG_CAPACITY);
+                sl = -1;
             }
         }
-        if (threadIdx.x < K) {
-            const int sl = sh_slot[threadIdx.x];
-            if (sl >= 0) {
-                uint8_t* msg = a.regions + (((int64_t)sh_e[threadIdx.x] * R + s) * a.cap + sl) * a.msg_bytes;
-                *reinterpret_cast<int4*>(msg) = make_int4(t, 0, 0, 0);
+        sh_slot[k] = sl;
+        a.slot_out[g * K + k] = sl;
+        if (sl >= 0) {
+            uint8_t* msg = a.regions + (((int64_t)ev * R + s) * a.cap + sl) * a.msg_bytes;
+            *reinterpret_cast<int4*>(msg) = make_int4(t, 0, 0, 0);
+        }
+    }
+    __syncthreads();
+    // ---- quantise once, store to every destination region ----------------------
+    for (int gi0 = 0; gi0 < ngroups; gi0 += blockDim.x) {
+        const int gi = gi0 + threadIdx.x;
+        const bool act = gi < ngroups;
+        if (gi0 > 0 && act) {  // later passes (H > 16 * blockDim)
+            p0 = ld_nc_na_v4(xr + gi * 16);
+            p1 = ld_nc_na_v4(xr + gi * 16 + 8);
+        }
+        float v[16];
+        const uint32_t uu[8] = {(uint32_t)p0.x, (uint32_t)p0.y, (uint32_t)p0.z, (uint32_t)p0.w,
+                                (uint32_t)p1.x, (uint32_t)p1.y, (uint32_t)p1.z, (uint32_t)p1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[2 * i] = __uint_as_float(uu[i] << 16);
+            v[2 * i + 1] = __uint_as_float(uu[i] & 0xffff0000u);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        // max over the 8 lanes holding one 128-channel block
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float scale = __fdiv_rn(amax, 448.0f);
+        uint32_t w4[4];
+        if (scale == 0.0f) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t c = 0;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) c |= ((__float_as_uint(v[4 * i + b]) >> 31) ? 0x80u : 0u) << (8 * b);
+                w4[i] = c;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t lo = e4m3x2(__fdiv_rn(v[4 * i], scale), __fdiv_rn(v[4 * i + 1], scale));
+                const uint32_t hi = e4m3x2(__fdiv_rn(v[4 * i + 2], scale), __fdiv_rn(v[4 * i + 3], scale));
+                w4[i] = (lo & 0xffffu) | (hi << 16);
+            }
+        }
+        if (act) {
+            const int4 codes = make_int4((int)w4[0], (int)w4[1], (int)w4[2], (int)w4[3]);
+            for (int k = 0; k < K; ++k) {
+                const int sl = sh_slot[k];
+                if (sl < 0) continue;
+                uint8_t* msg = a.regions + (((int64_t)sh_e[k] * R + s) * a.cap + sl) * a.msg_bytes;
+                st_na_v4(msg + 16 + (int64_t)gi * 16, codes);
+                if ((gi & 7) == 0) *reinterpret_cast<float*>(msg + 16 + H + (gi >> 3) * 4) = scale;
             }
         }
     }
-    (void)lane;
-    // ---- completion: the last CTA of this source publishes its counts -----------
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) is_last = atomicAdd(&a.done[s], 1u) == (uint32_t)(a.nblk - 1);
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) sh_hist[e] = 0;
+}
+
+// grid = R sources (launched as a programmatic dependent of ll_send_kernel).
+// Counts the source's entries per expert while the send runs, then waits for
+// the send grid to complete (griddepcontrol.wait: its writes are visible) and
+// publishes every count slot of the source, 0 included, with release stores.
+// Also re-arms the other ping-pong buffer's count slots of this source.
+__global__ void __launch_bounds__(256) ll_publish_kernel(LLSendArgs a) {
+    extern __shared__ int32_t sh_hist[];  // [E]
+    const int s = blockIdx.x;
+    const int E = a.E, R = a.R, K = a.K;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        sh_hist[e] = 0;
+        st_relaxed_gpu(a.other_counts + (int64_t)e * R + s, -1);
+    }
     __syncthreads();
     const int64_t* first = a.topk_idx + ((int64_t)s * a.T + a.t0) * K;
     for (int i = threadIdx.x; i < a.n * K; i += blockDim.x) {
@@ -193,12 +212,11 @@ __global__ void __launch_bounds__(kSendThreads) ll_send_kernel(LLSendArgs a) {
         if (e >= 0 && e < E) atomicAdd(&sh_hist[e], 1);
     }
     __syncthreads();
-    __threadfence();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         const int c = sh_hist[e];
         st_release_gpu(a.counts + (int64_t)e * R + s, c < a.cap ? c : a.cap);
     }
-    if (threadIdx.x == 0) a.done[s] = 0;  // re-arm for the next use of this buffer
 }
 
 struct LLRecvArgs {
@@ -233,17 +251,15 @@ __device__ int wait_count(const int32_t* p, int64_t limit_ns, uint32_t* status) 
     }
 }
 
-__device__ __forceinline__ int4 ld_cg_v4(const void* p) {
-    int4 v;
-    asm volatile("ld.global.cg.v4.s32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
 
 // grid = (R sources, E experts): CTA (s, e) waits for the counts of sources
 // 0..s of expert e (begin = exclusive prefix), then copies its messages.
 __global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(LLRecvArgs a) {
     __shared__ int sh_begin, sh_count;
     const int s = blockIdx.x, e = blockIdx.y;
+    // launched as a programmatic dependent of the count publisher: start once
+    // its grid (and every write before it) is complete
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int R = a.R, L = a.L, H = a.H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp == 0) {
@@ -279,13 +295,28 @@ __global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(LLRecvArgs a) {
     const int S = H / 128;
     const int64_t rows_per_expert = (int64_t)R * a.cap;
     const int nwarps = blockDim.x / 32;
+    const int nv = H / 16;
     for (int i = warp; i < count; i += nwarps) {
         const uint8_t* msg = a.regions + (((int64_t)e * R + s) * a.cap + i) * a.msg_bytes;
         const int64_t p = ((int64_t)d * L + l) * rows_per_expert + begin + i;
-        uint8_t* dx = a.packed_x + p * H;
-        for (int v = lane; v < H / 16; v += 32) st_na_v4(dx + (int64_t)v * 16, ld_cg_v4(msg + 16 + (int64_t)v * 16));
+        const int4* src = reinterpret_cast<const int4*>(msg + 16);
+        int4* dx = reinterpret_cast<int4*>(a.packed_x + p * H);
+        // issue a batch of loads before the stores that consume them
+        for (int v0 = 0; v0 < nv; v0 += 8 * 32) {
+            int4 buf[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int v = v0 + u * 32 + lane;
+                if (v < nv) buf[u] = __ldcg(src + v);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int v = v0 + u * 32 + lane;
+                if (v < nv) __stcs(dx + v, buf[u]);
+            }
+        }
         const float* sc = reinterpret_cast<const float*>(msg + 16 + H);
-        for (int v = lane; v < S; v += 32) a.packed_scales[p * S + v] = __ldcg(sc + v);
+        for (int v = lane; v < S; v += 32) __stcs(a.packed_scales + p * S + v, __ldcg(sc + v));
         if (lane == 0) {
             a.packed_src_info[p * 2] = s;
             a.packed_src_info[p * 2 + 1] = __ldcg(reinterpret_cast<const int32_t*>(msg));
@@ -417,13 +448,32 @@ extern "C" ep_status ep_ll_send(ep_ll_buffer* b, const void* x, const int64_t* t
     a.cap = b->cap;
     a.t0 = t0;
     a.n = n;
-    a.nblk = n > 0 ? n : 1;
+    a.nblk = n;
     a.msg_bytes = b->msg_bytes;
     a.status = b->status;
-    dim3 grid(a.nblk, a.R);
-    const size_t smem = sizeof(int32_t) * (size_t)a.E;
-    ll_send_kernel<<<grid, kSendThreads, smem, as_stream(stream)>>>(a);
-    EP_CHECK_LAUNCH("ll_send_kernel");
+    cudaStream_t s = as_stream(stream);
+    if (n > 0) {
+        // one thread per 16 channels (one pass) up to 1024 threads, whole warps
+        int threads = ((a.H / 16 + 31) / 32) * 32;
+        if (threads < 64) threads = 64;
+        if (threads > kSendThreads) threads = kSendThreads;
+        ll_send_kernel<<<dim3(n, a.R), threads, 0, s>>>(a);
+        EP_CHECK_LAUNCH("ll_send_kernel");
+    }
+    // counts after the data: a programmatic dependent launch overlaps the
+    // publisher's histogram with the send; its griddepcontrol.wait orders the
+    // count stores after every data store of the send grid
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(a.R);
+    lc.blockDim = dim3(256);
+    lc.dynamicSmemBytes = sizeof(int32_t) * (size_t)a.E;
+    lc.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    EP_CUDA(cudaLaunchKernelEx(&lc, ll_publish_kernel, a));
     return EP_OK;
 }
 
@@ -449,9 +499,17 @@ extern "C" ep_status ep_ll_recv(ep_ll_buffer* b, uint8_t* packed_x, float* packe
     a.msg_bytes = b->msg_bytes;
     a.timeout_ns = b->wait_timeout_ns;
     a.status = b->status;
-    dim3 grid(a.R, a.E);
-    ll_recv_kernel<<<grid, kRecvThreads, 0, as_stream(stream)>>>(a);
-    EP_CHECK_LAUNCH("ll_recv_kernel");
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(a.R, a.E);
+    lc.blockDim = dim3(kRecvThreads);
+    lc.dynamicSmemBytes = 0;
+    lc.stream = as_stream(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    EP_CUDA(cudaLaunchKernelEx(&lc, ll_recv_kernel, a));
     return EP_OK;
 }
 
