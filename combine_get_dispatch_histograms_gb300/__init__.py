@@ -61,12 +61,20 @@ def ll_size_hint(num_max_dispatch_tokens_per_rank: int, hidden: int, num_ranks: 
 class Handle(dict):
     """Device arrays of the dispatch handle plus the host counts of notify."""
 
+    _cs = None
+
+    def __setitem__(self, key, value):
+        self._cs = None
+        super().__setitem__(key, value)
+
     def c_struct(self) -> EpDispatchHandle:
-        h = EpDispatchHandle()
-        for name, _ in EpDispatchHandle._fields_:
-            t = self.get(name)
-            setattr(h, name, None if t is None else t.data_ptr())
-        return h
+        if self._cs is None:
+            h = EpDispatchHandle()
+            for name, _ in EpDispatchHandle._fields_:
+                t = self.get(name)
+                setattr(h, name, None if t is None else t.data_ptr())
+            self._cs = h
+        return self._cs
 
 
 class Context:
@@ -85,6 +93,9 @@ class Context:
         self._ctx = ctypes.c_void_p()
         with torch.cuda.device(self.device):
             check("ep_ctx_create", self.lib.ep_ctx_create(ctypes.byref(self.cfg), ctypes.byref(self._ctx)))
+        self._host_recv = (ctypes.c_int32 * num_ranks)()
+        self._host_exp = (ctypes.c_int32 * num_experts)()
+        self._host_tot = (ctypes.c_int32 * 3)()
 
     def close(self):
         if self._ctx:
@@ -146,9 +157,7 @@ class Context:
     def notify_dispatch(self, topk_idx: torch.Tensor, layout: dict, stream=None, handle: Optional[Handle] = None) -> Handle:
         _require_cuda(topk_idx)
         h = handle if handle is not None else self.alloc_handle()
-        host_recv = (ctypes.c_int32 * self.R)()
-        host_exp = (ctypes.c_int32 * self.E)()
-        host_tot = (ctypes.c_int32 * 3)()
+        host_recv, host_exp, host_tot = self._host_recv, self._host_exp, self._host_tot
         cs = h.c_struct()
         check("ep_notify_dispatch", self.lib.ep_notify_dispatch(
             self._ctx, _ptr(topk_idx), _ptr(layout["num_tokens_per_expert"]), _ptr(layout["num_tokens_per_rank"]),

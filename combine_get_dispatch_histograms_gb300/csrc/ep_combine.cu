@@ -47,7 +47,7 @@ __device__ __forceinline__ int4 f32x8_to_bf16(const float* f) {
 
 // MODE 0: flat (rank partials), 1: hierarchical (rank, node, final), 2: low-latency (k order)
 template <int KMAX, int MODE>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a) {
+__global__ void __launch_bounds__(kCombineThreads, KMAX <= 8 ? 3 : 1) combine_kernel(CombineArgs a) {
     __shared__ int64_t sh_row[kCombineWarps][KMAX];
     __shared__ float sh_w[kCombineWarps][KMAX];
     __shared__ uint8_t sh_brk[kCombineWarps][KMAX];  // bit0: new rank group, bit1: new node group

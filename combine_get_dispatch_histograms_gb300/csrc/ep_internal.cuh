@@ -90,7 +90,8 @@ struct ep_ctx {
     uint32_t* ws_notify_done;  // [1]
     uint32_t* status;          // [1]      device status word
     // pinned, device-mapped host block written by the notify kernel
-    int32_t* host_block;       // [R + R*L + 4]
+    int32_t* host_block;       // [R + R*L + 8]: counts, totals, status, sequence word
+    int32_t notify_epoch;      // sequence number of the last notify
     int32_t* host_block_dev;
     cudaEvent_t ev_counts;
     int64_t wait_timeout_ns;

@@ -15,6 +15,7 @@
 // All R virtual ranks are handled by one launch.  The exchange of counts
 // between ranks is a transpose read of the [R][R] matrix and the barrier of
 // the original design is stream order.
+#include <chrono>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -162,8 +163,9 @@ struct NotifyArgs {
     int32_t* part;   // [R][tiles][E + R + N]
     int32_t* ebase;  // [R][E]
     int32_t* sbase;  // [R][N]
-    int32_t* host;   // mapped: [R] num_recv, [R*L] per expert, [3] totals, [1] status
+    int32_t* host;   // mapped: [R] num_recv, [R*L] per expert, [3] totals, [1] status, [1] epoch
     uint32_t* status;
+    int32_t epoch;   // sequence number of this notify call
 };
 
 __device__ void notify_global_scan(const NotifyArgs& a) {
@@ -269,6 +271,9 @@ __device__ void notify_global_scan(const NotifyArgs& a) {
         a.host[R + E + 0] = sh_total_recv;
         a.host[R + E + 1] = a.h.perm_rank_base[R];
         a.host[R + E + 3] = (int32_t)atomicOr(a.status, 0u);
+        __threadfence_system();
+        // the host polls this word: it is written after every count above
+        *reinterpret_cast<volatile int32_t*>(a.host + R + E + 4) = a.epoch;
         __threadfence_system();
     }
 }
@@ -553,7 +558,7 @@ extern "C" ep_status ep_ctx_create(const ep_config* cfg, ep_ctx** out) {
     c->ws_notify_done = reinterpret_cast<uint32_t*>(b + o_nd);
     c->status = reinterpret_cast<uint32_t*>(b + o_st);
     e = cudaMemset(c->ws, 0, c->ws_bytes);
-    const size_t hb = sizeof(int32_t) * (size_t)(R + E + 4);
+    const size_t hb = sizeof(int32_t) * (size_t)(R + E + 8);
     if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&c->host_block), hb, cudaHostAllocMapped);
     if (e == cudaSuccess) e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->host_block_dev), c->host_block, 0);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_counts, cudaEventDisableTiming);
@@ -720,6 +725,7 @@ extern "C" ep_status ep_notify_dispatch(ep_ctx* c, const int64_t* topk_idx, cons
     a.sbase = c->ws_sbase;
     a.host = c->host_block_dev;
     a.status = c->status;
+    a.epoch = ++c->notify_epoch;
     const int W = a.E + a.R + a.N;
     cudaStream_t s = as_stream(stream);
     const int nblk = a.R * c->tiles.tiles_per_src + 1;
@@ -730,10 +736,30 @@ extern "C" ep_status ep_notify_dispatch(ep_ctx* c, const int64_t* topk_idx, cons
     notify_position_kernel<<<grid, kTileTokens, notify_position_smem(c), s>>>(a);
     EP_CHECK_LAUNCH("notify_position_kernel");
     c->last_launches = 2;
-    // the one host synchronisation of the normal path: the receive counts
-    EP_CUDA(cudaEventSynchronize(c->ev_counts));
+    // the one host synchronisation of the normal path: the receive counts.
+    // Poll the CPU-mapped sequence word the count kernel writes last (cheaper
+    // than an event wake-up); the event bounds the poll and reports errors.
     volatile int32_t* hb = c->host_block;
     const int R = a.R, E = a.E;
+    {
+        const auto t0 = std::chrono::steady_clock::now();
+        unsigned spins = 0;
+        while (hb[R + E + 4] != a.epoch) {
+            if ((++spins & 1023u) == 0) {
+                const cudaError_t q = cudaEventQuery(c->ev_counts);
+                if (q == cudaSuccess) {
+                    if (hb[R + E + 4] != a.epoch) return set_error(EP_ERR_CUDA, "notify counts were not published");
+                    break;
+                }
+                if (q != cudaErrorNotReady) return cuda_error(q, "notify_count_kernel");
+                if (std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(2)) {
+                    EP_CUDA(cudaEventSynchronize(c->ev_counts));  // long wait: block instead of spinning
+                    if (hb[R + E + 4] != a.epoch) return set_error(EP_ERR_CUDA, "notify counts were not published");
+                    break;
+                }
+            }
+        }
+    }
     for (int d = 0; d < R; ++d) host_num_recv[d] = hb[d];
     if (host_num_recv_per_expert)
         for (int e = 0; e < E; ++e) host_num_recv_per_expert[e] = hb[R + e];
