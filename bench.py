@@ -31,9 +31,13 @@ METRIC = "dispatch+combine tokens/s and effective HBM GB/s (% of ~8 TB/s); LL µ
 L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes per launch from the ncu capture named in "source", for the
-# kernel bench.py reports as dominant (null until captured for this kernel).
-TRAFFIC = {}
+# DRAM bytes (read + write) per launch of the dominant kernel, from the ncu
+# capture named in "source" (a T=1024 case of the same kernel, scaled to a full
+# launch by the rows it moves); null for kernels not captured since they changed.
+TRAFFIC = {
+    ("prefill", "permute"): {"bytes": 6.074e9,
+                             "source": "profiles/kernels_prefill_t1024_ncu_full.md (T=1024 capture x 4.024)"},
+}
 
 
 def measured_hbm_gbs():
@@ -50,13 +54,22 @@ def measured_hbm_gbs():
 # algorithmic bytes per unit of work (each row read or written once)
 # ---------------------------------------------------------------------------
 
-def algo_bytes(H, K, tokens, copies, pairs):
+def algo_bytes(H, K, tokens, copies, pairs, staged=0):
+    """staged = node copies of the hierarchical dispatch (0: flat): stage A reads
+    each token once and writes one row per destination node, stage B reads each
+    staged row once and writes one row per destination rank."""
     row = 2 * H
+    dispatch = (tokens + copies) * row if not staged else (tokens + 2 * staged + copies) * row
     return {
-        "dispatch": (tokens + copies) * row,
+        "dispatch": dispatch,
         "permute": (copies + pairs) * row,
         "combine": (pairs + tokens) * row + tokens * K * 8,
     }
+
+
+def pct(xs, q):
+    xs = sorted(xs)
+    return xs[min(len(xs) - 1, max(0, int(round(q * (len(xs) - 1)))))]
 
 
 def ll_algo_bytes(H, tokens, pairs):
@@ -157,6 +170,43 @@ def oracle_sample(workload, budget_s: float, min_s: float):
                       f"single-threaded plain C oracle, {t_total:.1f} s"}
 
 
+def _oracle_worker(args):
+    name, T, seed, budget = args
+    from combine_get_dispatch_histograms_gb300 import inputs
+    w = inputs.WORKLOADS[name].replace(T=T)
+    import oracle
+    tokens, t_total = 0, 0.0
+    while True:
+        x, idx, wts = inputs.make_inputs(w, seed=seed)
+        t = time.perf_counter()
+        oracle.run_normal(x, idx, wts, w.R, w.E, w.num_channels)
+        t_total += time.perf_counter() - t
+        tokens += w.R * w.T
+        seed += 1000
+        if t_total >= budget:
+            return tokens, t_total
+
+
+def oracle_parallel(workload, seconds: float):
+    """The same oracle, one independent sample stream per host core (spawned
+    processes), aggregate tokens/s."""
+    import multiprocessing as mp
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    T = 128 if workload.H >= 4096 else 1024
+    ctx = mp.get_context("spawn")
+    t0 = time.perf_counter()
+    with ctx.Pool(cores) as pool:
+        res = pool.map(_oracle_worker, [(workload.name, T, 500 + i, seconds) for i in range(cores)])
+    wall = time.perf_counter() - t0
+    tokens = sum(r[0] for r in res)
+    busy = max(r[1] for r in res)
+    return {"value": tokens / busy, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{tokens} tokens over {cores} spawned processes, batches of R={workload.R} x T={T}, "
+                      f"{busy:.1f} s of oracle time per process ({wall:.1f} s wall incl. input generation)"}
+
+
 def run_reference(args, workload):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -190,7 +240,7 @@ def run_reference(args, workload):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill", choices=["prefill", "skewed", "hier"])
@@ -332,11 +382,41 @@ def main():
         lname = ["ll_send", "ll_recv", "ll_combine"]
         lper = {n: statistics.median(e[j].elapsed_time(e[j + 1]) for e in lev) for j, n in enumerate(lname)}
         layer_us = statistics.median(e[0].elapsed_time(e[3]) for e in lev) * 1e3
+        # the same layer captured once in a CUDA graph and replayed (static shapes,
+        # no host sync, no allocation inside the layer)
+        graph_us = None
+        try:
+            gs = torch.cuda.Stream()
+            gs.wait_stream(stream)
+            with torch.cuda.stream(gs):
+                buf.dispatch(d_x, d_idx_d, out=pk)  # warm the side stream
+                buf.combine(y_ll, d_idx_d, d_w_d, pk, out=d_out)
+            gs.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=gs):
+                buf.dispatch(d_x, d_idx_d, out=pk)
+                buf.combine(y_ll, d_idx_d, d_w_d, pk, out=d_out)
+            torch.cuda.synchronize()
+            gt = []
+            for i in range(args.steps + 2):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if i >= 2:
+                    gt.append(e0.elapsed_time(e1))
+            buf.check()
+            graph_us = round(statistics.median(gt) * 1e3, 2)
+            del graph
+        except Exception as exc:  # reported, not hidden
+            graph_us = f"capture failed: {exc}"
         d_pairs = int((d_idx >= 0).sum())
         lbytes = ll_algo_bytes(dw.H, dw.R * dw.T, d_pairs)
         peak, _ = measured_hbm_gbs()
         ll = {"workload": "decode", "R": dw.R, "T": dw.T, "H": dw.H, "cap": dw.ll_cap,
-              "us_per_layer": round(layer_us, 2),
+              "us_per_layer": round(layer_us, 2), "us_per_layer_cuda_graph": graph_us,
               "kernels": {n: {"us": round(lper[n] * 1e3, 2), "algo_bytes": lbytes[n],
                               "GBps": round(lbytes[n] / (lper[n] * 1e-3) / 1e9, 1),
                               "frac": round(lbytes[n] / (lper[n] * 1e-3) / 1e9 / peak, 3)} for n in lname},
@@ -391,11 +471,12 @@ def main():
 
     # ---- roofline of the dominant kernel ------------------------------------------
     peak, peak_kind = measured_hbm_gbs()
-    ab = algo_bytes(H, K, tokens, copies, pairs)
+    ab = algo_bytes(H, K, tokens, copies, pairs, handle.num_stage_rows if hier else 0)
     med = {n: statistics.median(per[n]) for n in names}
     kernels = {}
     for n in names:
-        entry = {"us": round(med[n] * 1e3, 2)}
+        entry = {"us": round(med[n] * 1e3, 2), "p10_us": round(pct(per[n], 0.1) * 1e3, 2),
+                 "p90_us": round(pct(per[n], 0.9) * 1e3, 2)}
         if n in ab:
             gbs = ab[n] / (med[n] * 1e-3) / 1e9
             entry.update({"algo_bytes": ab[n], "GBps": round(gbs, 1), "frac": round(gbs / peak, 3)})
@@ -403,15 +484,20 @@ def main():
     dom = max(ab, key=lambda n: med[n])
     dom_avg_ms = sum(per[dom]) / len(per[dom])
     achieved = ab[dom] / (dom_avg_ms * 1e-3) / 1e9
-    tr = TRAFFIC.get((w.name, dom))
+    tr = TRAFFIC.get((w.name, dom)) if not args.tokens else None
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                 "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "algo_bytes_per_launch": ab[dom], "traffic": tr}
+                "algo_bytes_per_launch": ab[dom], "traffic": tr["bytes"] if tr else None,
+                "traffic_source": tr["source"] if tr else None}
 
     cpu = None
-    if not args.no_cpu and world >= 1:
+    if not args.no_cpu:
         cpu = oracle_sample(w, budget_s=25.0, min_s=10.0)
+        try:
+            cpu["all_cores"] = oracle_parallel(w, 8.0)
+        except Exception as exc:
+            cpu["all_cores"] = f"unavailable: {exc}"
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,

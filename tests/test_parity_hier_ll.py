@@ -142,3 +142,42 @@ def test_low_latency_workload_shapes_small():
             sent = orc.ll_send(x, idx, R, E, cap, t0, n)
             o_pk = orc.ll_pack(sent, R, E, H, cap)
             check_ll_microbatch(pk, sent, o_pk, R, E, K, T, H, cap, t0, n, idx)
+
+
+def test_low_latency_layer_in_cuda_graph():
+    """The low-latency layer (send, receive, combine) has static shapes and no
+    host synchronisation: captured once in a CUDA graph, each replay gives the
+    eager result."""
+    R, E, K, T, H, cap = 8, 64, 4, 24, 256, 24
+    idx = inputs.random_topk(R, E, K, T, 21, 0.1)
+    x = inputs.random_x(R, T, H, 21)
+    w = inputs.random_weights(R, T, K, 21)
+    from combine_get_dispatch_histograms_gb300 import LLBuffer
+    buf = LLBuffer(R, E, K, T, H, cap)
+    xd, idxd, wd = x.cuda(), idx.cuda(), w.cuda()
+    sent = orc.ll_send(x, idx, R, E, cap)
+    o_pk = orc.ll_pack(sent, R, E, H, cap)
+    y = orc.ll_dequant(o_pk["packed_x"], o_pk["packed_scales"])
+    yd = torch.from_numpy(y.view(np.int16)).view(torch.bfloat16).cuda()
+    o_out = orc.ll_combine(y, idx, w, sent["slot"], o_pk["layout_range"], R, E, cap)
+    pk = buf.alloc_packed()
+    out = torch.zeros(R, T, H, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        buf.dispatch(xd, idxd, out=pk)
+        buf.combine(yd, idxd, wd, pk, out=out)
+    s.synchronize()
+    eq(out, o_out, "eager")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        buf.dispatch(xd, idxd, out=pk)
+        buf.combine(yd, idxd, wd, pk, out=out)
+    for _ in range(3):
+        out.zero_()
+        pk["packed_recv_count"].fill_(-5)
+        g.replay()
+        torch.cuda.synchronize()
+        buf.check()
+        eq(out, o_out, "graph replay")
+        eq(pk["packed_recv_count"], o_pk["packed_recv_count"], "graph replay counts")
