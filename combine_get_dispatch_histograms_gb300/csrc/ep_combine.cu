@@ -184,18 +184,29 @@ ep_status launch_combine(const CombineArgs& a, int mode, int num_sms, cudaStream
     const int64_t n_tok = (int64_t)a.R * a.n;
     if (n_tok <= 0) return EP_OK;
     CombineArgs b = a;
-    // channel slices per token: aim for about 48 warps per SM, at least one
-    // 16-byte vector per lane per slice
+    // Work items are (token, channel slice).  The grid holds `conc` resident
+    // warps; pick the number of slices per token (1..8, at least one 16-byte
+    // vector per lane per slice) whose items fill the last round of warps best,
+    // preferring fewer slices (each slice reloads the token's entries).
     const int nvec = a.H / 8;
-    const int64_t target = (int64_t)num_sms * 48;
-    int splits = (int)((target + n_tok - 1) / n_tok);
-    if (splits > nvec / 32) splits = nvec / 32;
-    if (splits > 8) splits = 8;
-    if (splits < 1) splits = 1;
+    const int64_t conc = (int64_t)num_sms * 3 * kCombineWarps;
+    int max_splits = nvec / 32 < 8 ? nvec / 32 : 8;
+    if (max_splits < 1) max_splits = 1;
+    int splits = 1;
+    double best = -1.0;
+    for (int sp = 1; sp <= max_splits; ++sp) {
+        const int64_t items = n_tok * sp;
+        const int64_t rounds = (items + conc - 1) / conc;
+        const double eff = (double)items / (double)(rounds * conc);
+        if (eff > best + 0.03) {
+            best = eff;
+            splits = sp;
+        }
+    }
     b.splits = splits;
     const int64_t items = n_tok * splits;
     int64_t want = (items + kCombineWarps - 1) / kCombineWarps;
-    const int64_t cap = (int64_t)num_sms * 16;
+    const int64_t cap = (int64_t)num_sms * 3;
     const int grid = (int)(want < cap ? want : cap);
     cudaError_t e = mode == 0 ? launch_mode<0>(b, grid, s) : mode == 1 ? launch_mode<1>(b, grid, s) : launch_mode<2>(b, grid, s);
     if (e != cudaSuccess) return cuda_error(e, "combine kernel");

@@ -21,6 +21,7 @@
 // after the data, 0 included.  The receive kernel polls each count with
 // ld.acquire under a time limit and packs the messages.
 #include <cuda_fp8.h>
+#include <cstdlib>
 
 #include "ep_internal.cuh"
 #include "ep_combine.cuh"
@@ -37,11 +38,12 @@ struct ep_ll_buffer {
     uint32_t* status;
     int cur;
     int64_t wait_timeout_ns;
+    int send_ctas_per_sm;    // send kernel launch shape
+    size_t send_smem_bytes;
 };
 
 namespace ep {
 
-constexpr int kSendThreads = 1024;
 constexpr int kRecvThreads = 128;
 
 struct LLSendArgs {
@@ -62,132 +64,190 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
     return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
-// grid = (n tokens, R sources), one CTA per token.  All loads of the CTA (its
-// own top-k entries, the source's earlier entries of the microbatch, the x row)
-// are issued before the first barrier; the slots come from shared-memory
-// counts; the token is quantised once and stored to its K regions.  No fence
-// or atomic on global memory: the counts are published by ll_publish_kernel.
-constexpr int kPriorPerThread = 8;
+// Persistent send: CTA c owns the contiguous tokens [q0, q1) of the flattened
+// (source, token) order.  Thread 0 streams their x rows global -> shared with
+// cp.async.bulk, `stages` tokens ahead (one mbarrier per stage).  A running
+// per-expert count of the current source in shared memory gives each entry's
+// slot (initialised once from the source's earlier tokens).  All threads
+// quantise the staged row into a message in shared memory (header, e4m3
+// codes, fp32 scales); thread 0 then writes that message to each of the
+// token's K regions with cp.async.bulk shared -> global.  The counts are
+// published afterwards by ll_publish_kernel.
+constexpr int kSendMaxStages = 8;
 
-__global__ void __launch_bounds__(1024) ll_send_kernel(LLSendArgs a) {
-    __shared__ int sh_e[kMaxTopk];
-    __shared__ int sh_cnt[kMaxTopk];
-    __shared__ int sh_slot[kMaxTopk];
-    const int s = blockIdx.y, j = blockIdx.x;  // j-th token of the microbatch
-    const int K = a.K, R = a.R, E = a.E, H = a.H;
-    // let the publish kernel start its own (independent) work early
+__host__ __device__ inline size_t ll_send_fixed_smem(int E) {
+    size_t off = kSendMaxStages * sizeof(uint64_t) + sizeof(int32_t) * ((size_t)E + 4 * kMaxTopk + 4);
+    return (off + 127) & ~size_t(127);
+}
+
+__global__ void __launch_bounds__(256) ll_send_kernel(LLSendArgs a, int stages, int64_t timeout_ns) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    int32_t* cnt = reinterpret_cast<int32_t*>(bar + kSendMaxStages);  // [E]
+    int32_t* sh_e2 = cnt + a.E;                                         // [2][kMaxTopk] by token parity
+    int32_t* sh_slot2 = sh_e2 + 2 * kMaxTopk;                           // [2][kMaxTopk]
+    int32_t* sh_flag = sh_slot2 + 2 * kMaxTopk;                         // [1] abort
+    const int R = a.R, E = a.E, K = a.K, H = a.H, n = a.n;
+    const int64_t row_bytes = (int64_t)H * 2;
+    uint8_t* xs = smem + ll_send_fixed_smem(E);                        // [stages][row_bytes]
+    uint8_t* msgs = xs + (size_t)stages * row_bytes;                    // [2][msg_bytes]
+    const int64_t total = (int64_t)R * n;
+    const int64_t q0 = total * blockIdx.x / gridDim.x, q1 = total * (blockIdx.x + 1) / gridDim.x;
+    const int tid = threadIdx.x;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int t = a.t0 + j;
-    const int64_t g = (int64_t)s * a.T + t;
-    const int64_t* first = a.topk_idx + ((int64_t)s * a.T + a.t0) * K;
-    const int prior = j * K;
-    // ---- loads ---------------------------------------------------------------------
-    if (threadIdx.x < K) {
-        const int64_t e = a.topk_idx[g * K + threadIdx.x];
-        int ev = -1;
-        if (e >= 0 && e < E) ev = (int)e;
-        else if (e != -1) flag(a.status, FLAG_INVALID_TOPK);
-        sh_e[threadIdx.x] = ev;
-        sh_cnt[threadIdx.x] = 0;
+    auto token_g = [&](int64_t q) -> int64_t { return (int64_t)(q / n) * a.T + a.t0 + (int)(q % n); };
+    auto issue_load = [&](int64_t q) {
+        const int st = (int)((q - q0) % stages);
+        mbar_arrive_expect_tx(&bar[st], (uint32_t)row_bytes);
+        bulk_g2s(xs + (size_t)st * row_bytes, a.x + token_g(q) * H, (uint32_t)row_bytes, &bar[st]);
+    };
+    if (tid == 0) {
+        for (int st = 0; st < stages; ++st) mbar_init(&bar[st], 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        for (int64_t q = q0; q < q1 && q < q0 + stages; ++q) issue_load(q);
+        sh_flag[0] = 0;
     }
-    int pe[kPriorPerThread];
-#pragma unroll
-    for (int u = 0; u < kPriorPerThread; ++u) {
-        const int i = threadIdx.x + u * blockDim.x;
-        const int64_t e = i < prior ? first[i] : -1;
-        pe[u] = (e >= 0 && e < E) ? (int)e : -1;
-    }
-    const int ngroups = H / 16;  // 16 channels per thread per pass; 8 groups per scale block
-    const uint16_t* xr = a.x + g * H;
-    int4 p0 = make_int4(0, 0, 0, 0), p1 = make_int4(0, 0, 0, 0);
-    if ((int)threadIdx.x < ngroups) {
-        p0 = ld_nc_na_v4(xr + threadIdx.x * 16);
-        p1 = ld_nc_na_v4(xr + threadIdx.x * 16 + 8);
-    }
-    __syncthreads();
-    // ---- slots: earlier entries of this source with the same expert ----------------
-#pragma unroll
-    for (int u = 0; u < kPriorPerThread; ++u)
-        if (pe[u] >= 0)
-            for (int k = 0; k < K; ++k)
-                if (sh_e[k] == pe[u]) atomicAdd(&sh_cnt[k], 1);
-    for (int i = threadIdx.x + kPriorPerThread * blockDim.x; i < prior; i += blockDim.x) {
-        const int64_t e = first[i];
-        if (e < 0 || e >= E) continue;
-        for (int k = 0; k < K; ++k)
-            if (sh_e[k] == (int)e) atomicAdd(&sh_cnt[k], 1);
-    }
-    __syncthreads();
-    if (threadIdx.x < K) {
-        const int k = threadIdx.x;
-        const int ev = sh_e[k];
-        int sl = -1;
-        if (ev >= 0) {
-            sl = sh_cnt[k];
-            for (int k2 = 0; k2 < k; ++k2) sl += (sh_e[k2] == ev);
-            if (sl >= a.cap) {
-                flag(a.status, FLAG_CAPACITY);
-                sl = -1;
+    int cur_s = -1;
+    int64_t nx_e = -1;  // next token's entry (threads < K), loaded one token ahead
+    if (q0 < q1 && tid < K) nx_e = a.topk_idx[token_g(q0) * K + tid];
+    int64_t next_load = q0 + stages < q1 ? q0 + stages : q1;  // thread 0: first token not yet loaded
+    int64_t q_stop = q1;
+    for (int64_t q = q0; q < q1; ++q) {
+        const int64_t i = q - q0;
+        // entries and slots of this token live in the buffer of its parity, so
+        // that thread 0 can still read the previous token's while the others
+        // move on
+        int32_t* sh_e = sh_e2 + (i & 1) * kMaxTopk;
+        int32_t* sh_slot = sh_slot2 + (i & 1) * kMaxTopk;
+        const int s = (int)(q / n), j = (int)(q % n), t = a.t0 + j;
+        const int64_t g = (int64_t)s * a.T + t;
+        const int64_t my_e = nx_e;
+        if (q + 1 < q1 && tid < K) nx_e = a.topk_idx[token_g(q + 1) * K + tid];
+        if (s != cur_s) {
+            // counts of this source's earlier tokens in the microbatch, per expert
+            __syncthreads();
+            for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+            __syncthreads();
+            const int64_t* first = a.topk_idx + ((int64_t)s * a.T + a.t0) * K;
+            for (int p = tid; p < j * K; p += blockDim.x) {
+                const int64_t e = first[p];
+                if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
             }
+            cur_s = s;
         }
-        sh_slot[k] = sl;
-        a.slot_out[g * K + k] = sl;
-        if (sl >= 0) {
-            uint8_t* msg = a.regions + (((int64_t)ev * R + s) * a.cap + sl) * a.msg_bytes;
-            *reinterpret_cast<int4*>(msg) = make_int4(t, 0, 0, 0);
+        if (tid < K) {
+            int ev = -1;
+            if (my_e >= 0 && my_e < E) ev = (int)my_e;
+            else if (my_e != -1) flag(a.status, FLAG_INVALID_TOPK);
+            sh_e[tid] = ev;
         }
-    }
-    __syncthreads();
-    // ---- quantise once, store to every destination region ----------------------
-    for (int gi0 = 0; gi0 < ngroups; gi0 += blockDim.x) {
-        const int gi = gi0 + threadIdx.x;
-        const bool act = gi < ngroups;
-        if (gi0 > 0 && act) {  // later passes (H > 16 * blockDim)
-            p0 = ld_nc_na_v4(xr + gi * 16);
-            p1 = ld_nc_na_v4(xr + gi * 16 + 8);
-        }
-        float v[16];
-        const uint32_t uu[8] = {(uint32_t)p0.x, (uint32_t)p0.y, (uint32_t)p0.z, (uint32_t)p0.w,
-                                (uint32_t)p1.x, (uint32_t)p1.y, (uint32_t)p1.z, (uint32_t)p1.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            v[2 * i] = __uint_as_float(uu[i] << 16);
-            v[2 * i + 1] = __uint_as_float(uu[i] & 0xffff0000u);
-        }
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        // max over the 8 lanes holding one 128-channel block
-#pragma unroll
-        for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float scale = __fdiv_rn(amax, 448.0f);
-        uint32_t w4[4];
-        if (scale == 0.0f) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                uint32_t c = 0;
-#pragma unroll
-                for (int b = 0; b < 4; ++b) c |= ((__float_as_uint(v[4 * i + b]) >> 31) ? 0x80u : 0u) << (8 * b);
-                w4[i] = c;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t lo = e4m3x2(__fdiv_rn(v[4 * i], scale), __fdiv_rn(v[4 * i + 1], scale));
-                const uint32_t hi = e4m3x2(__fdiv_rn(v[4 * i + 2], scale), __fdiv_rn(v[4 * i + 3], scale));
-                w4[i] = (lo & 0xffffu) | (hi << 16);
-            }
-        }
-        if (act) {
-            const int4 codes = make_int4((int)w4[0], (int)w4[1], (int)w4[2], (int)w4[3]);
+        __syncthreads();
+        if (tid == 0) {
             for (int k = 0; k < K; ++k) {
-                const int sl = sh_slot[k];
-                if (sl < 0) continue;
-                uint8_t* msg = a.regions + (((int64_t)sh_e[k] * R + s) * a.cap + sl) * a.msg_bytes;
-                st_na_v4(msg + 16 + (int64_t)gi * 16, codes);
+                const int ev = sh_e[k];
+                int sl = -1;
+                if (ev >= 0) {
+                    sl = cnt[ev];
+                    cnt[ev] = sl + 1;
+                    if (sl >= a.cap) {
+                        flag(a.status, FLAG_CAPACITY);
+                        sl = -1;
+                    }
+                }
+                sh_slot[k] = sl;
+                a.slot_out[g * K + k] = sl;
+            }
+        }
+        // the staged x row of this token
+        const int st = (int)(i % stages);
+        if (!mbar_wait_bounded(&bar[st], (uint32_t)((i / stages) & 1), timeout_ns)) {
+            flag(a.status, FLAG_TIMEOUT);
+            atomicExch(sh_flag, 1);
+        }
+        __syncthreads();
+        if (sh_flag[0]) {
+            q_stop = q;
+            break;
+        }
+        // ---- quantise into the message buffer ----------------------------------
+        uint8_t* msg = msgs + (size_t)(i & 1) * a.msg_bytes;
+        const uint8_t* xrow = xs + (size_t)st * row_bytes;
+        const int ngroups = H / 16;
+        for (int gi0 = 0; gi0 < ngroups; gi0 += blockDim.x) {
+            const int gi = gi0 + tid;
+            const bool act = gi < ngroups;
+            float v[16];
+            if (act) {
+                const int4 p0 = *reinterpret_cast<const int4*>(xrow + (size_t)gi * 32);
+                const int4 p1 = *reinterpret_cast<const int4*>(xrow + (size_t)gi * 32 + 16);
+                const uint32_t uu[8] = {(uint32_t)p0.x, (uint32_t)p0.y, (uint32_t)p0.z, (uint32_t)p0.w,
+                                        (uint32_t)p1.x, (uint32_t)p1.y, (uint32_t)p1.z, (uint32_t)p1.w};
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    v[2 * u] = __uint_as_float(uu[u] << 16);
+                    v[2 * u + 1] = __uint_as_float(uu[u] & 0xffff0000u);
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < 16; ++u) v[u] = 0.0f;
+            }
+            float amax = 0.0f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) amax = fmaxf(amax, fabsf(v[u]));
+            // max over the 8 lanes holding one 128-channel block
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const float scale = __fdiv_rn(amax, 448.0f);
+            uint32_t w4[4];
+            if (scale == 0.0f) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint32_t c = 0;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) c |= ((__float_as_uint(v[4 * u + b]) >> 31) ? 0x80u : 0u) << (8 * b);
+                    w4[u] = c;
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t lo = e4m3x2(__fdiv_rn(v[4 * u], scale), __fdiv_rn(v[4 * u + 1], scale));
+                    const uint32_t hi = e4m3x2(__fdiv_rn(v[4 * u + 2], scale), __fdiv_rn(v[4 * u + 3], scale));
+                    w4[u] = (lo & 0xffffu) | (hi << 16);
+                }
+            }
+            if (act) {
+                *reinterpret_cast<int4*>(msg + 16 + (size_t)gi * 16) =
+                    make_int4((int)w4[0], (int)w4[1], (int)w4[2], (int)w4[3]);
                 if ((gi & 7) == 0) *reinterpret_cast<float*>(msg + 16 + H + (gi >> 3) * 4) = scale;
             }
         }
+        if (tid == 0) *reinterpret_cast<int4*>(msg) = make_int4(t, 0, 0, 0);
+        fence_proxy_async_smem();  // the message is read by the bulk copies below
+        __syncthreads();
+        if (tid == 0) {
+            for (int k = 0; k < K; ++k) {
+                const int sl = sh_slot[k];
+                if (sl < 0) continue;
+                bulk_s2g(a.regions + (((int64_t)sh_e[k] * R + s) * a.cap + sl) * a.msg_bytes, msg,
+                         (uint32_t)a.msg_bytes);
+            }
+            bulk_commit();
+            // the x stage of this token is free again: stream the token `stages` ahead
+            if (q + stages < q1) {
+                fence_proxy_async_smem();
+                issue_load(q + stages);
+                next_load = q + stages + 1;
+            }
+            // the message buffer of the previous token must be read out before reuse
+            bulk_wait_read<1>();
+        }
+    }
+    if (tid == 0) {
+        bulk_wait_all();
+        // after an aborted wait, let the loads still in flight land before leaving
+        for (int64_t qq = q_stop; qq < next_load; ++qq)
+            mbar_wait_bounded(&bar[(qq - q0) % stages], (uint32_t)(((qq - q0) / stages) & 1), timeout_ns);
     }
 }
 
@@ -352,7 +412,8 @@ extern "C" ep_status ep_ll_buffer_create(const ep_config* cfg, int cap, ep_ll_bu
     const int R = cfg->num_ranks, E = cfg->num_experts, H = cfg->hidden, K = cfg->num_topk;
     if (R < 1 || R > kMaxRanks || E < 1 || E > kMaxExperts || E % R || K < 1 || K > kMaxTopk || cfg->num_tokens < 0)
         return set_error(EP_ERR_INVALID_ARG, "bad low-latency configuration (R %d, E %d, K %d)", R, E, K);
-    if (H < 128 || H % 128) return set_error(EP_ERR_INVALID_ARG, "hidden %d must be a positive multiple of 128", H);
+    if (H < 128 || H % 128 || H > 16384)
+        return set_error(EP_ERR_INVALID_ARG, "hidden %d must be a multiple of 128 in [128, 16384]", H);
     if (cap < 1 || cap > 4096) return set_error(EP_ERR_INVALID_ARG, "cap %d outside [1, 4096]", cap);
     ep_ll_buffer* b = new ep_ll_buffer();
     b->cfg = *cfg;
@@ -361,6 +422,15 @@ extern "C" ep_status ep_ll_buffer_create(const ep_config* cfg, int cap, ep_ll_bu
     b->msg_bytes = ep_ll_message_bytes(H);
     b->cur = 1;  // the first send flips to buffer 0
     b->wait_timeout_ns = 100000000ll;
+    b->send_ctas_per_sm = 3;
+    b->send_smem_bytes = 72 * 1024;
+    if (const char* v = getenv("EP_LL_SEND_CTAS_PER_SM")) b->send_ctas_per_sm = atoi(v) > 0 ? atoi(v) : 3;
+    if (const char* v = getenv("EP_LL_SEND_SMEM_KB")) b->send_smem_bytes = (size_t)(atoi(v) > 16 ? atoi(v) : 72) * 1024;
+    {
+        // room for two messages, the fixed part and at least two staged rows
+        const size_t need = ll_send_fixed_smem(E) + 2 * (size_t)ep_ll_message_bytes(H) + 2 * (size_t)H * 2;
+        if (b->send_smem_bytes < need) b->send_smem_bytes = need;
+    }
     cudaError_t e = cudaGetDevice(&b->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&b->num_sms, cudaDevAttrMultiProcessorCount, b->device);
     const int64_t one = ll_one_buffer_bytes(cap, H, R, E);
@@ -453,11 +523,16 @@ extern "C" ep_status ep_ll_send(ep_ll_buffer* b, const void* x, const int64_t* t
     a.status = b->status;
     cudaStream_t s = as_stream(stream);
     if (n > 0) {
-        // one thread per 16 channels (one pass) up to 1024 threads, whole warps
-        int threads = ((a.H / 16 + 31) / 32) * 32;
-        if (threads < 64) threads = 64;
-        if (threads > kSendThreads) threads = kSendThreads;
-        ll_send_kernel<<<dim3(n, a.R), threads, 0, s>>>(a);
+        const int64_t row_bytes = (int64_t)a.H * 2;
+        const size_t fixed = ll_send_fixed_smem(a.E) + 2 * (size_t)a.msg_bytes;
+        int stages = (int)((b->send_smem_bytes - fixed) / row_bytes);
+        if (stages > kSendMaxStages) stages = kSendMaxStages;
+        if (stages < 2) stages = 2;
+        const size_t smem = fixed + (size_t)stages * row_bytes;
+        int64_t grid = (int64_t)b->num_sms * b->send_ctas_per_sm;
+        if (grid > (int64_t)a.R * n) grid = (int64_t)a.R * n;
+        EP_CUDA(cudaFuncSetAttribute(ll_send_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        ll_send_kernel<<<(int)grid, 256, smem, s>>>(a, stages, 2000000000ll);
         EP_CHECK_LAUNCH("ll_send_kernel");
     }
     // counts after the data: a programmatic dependent launch overlaps the
