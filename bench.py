@@ -426,44 +426,95 @@ def main():
     clocks = sampler.stop()
 
     # ---- end to end through the public API with host buffers ------------------------
+    # Every step copies its inputs (x, topk_idx, topk_weights) from pinned host
+    # memory and its output back, inside the timed region.  Steps are pipelined
+    # the way a serving loop would run them: the inputs of step k+1 go up on a
+    # copy stream and the output of step k-1 comes down on another while step k
+    # computes (two slots of device inputs and outputs).
     e2e = None
     if not args.no_e2e:
         x_h = x.cpu().pin_memory()
         i_h = topk_idx.pin_memory()
         w_h = topk_w.pin_memory()
-        out_h = torch.empty(R, T, H, dtype=torch.bfloat16).pin_memory()
-        x_dev = torch.empty_like(x)
-        i_dev = torch.empty_like(idx_d)
-        w_dev = torch.empty_like(w_d)
+        out_h = [torch.empty(R, T, H, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        x_dev = [torch.empty_like(x) for _ in range(2)]
+        i_dev = [torch.empty_like(idx_d) for _ in range(2)]
+        w_dev = [torch.empty_like(w_d) for _ in range(2)]
+        out_dev = [torch.empty_like(out) for _ in range(2)]
+        up, down = torch.cuda.Stream(), torch.cuda.Stream()
+        ev = lambda: torch.cuda.Event()
+        in_ready = [ev() for _ in range(2)]
+        done = [ev() for _ in range(2)]
+        copied = [ev() for _ in range(2)]
+        for e_ in done + copied:
+            e_.record(stream)
 
-        def e2e_step():
-            x_dev.copy_(x_h, non_blocking=True)
-            i_dev.copy_(i_h, non_blocking=True)
-            w_dev.copy_(w_h, non_blocking=True)
-            ctx.get_dispatch_layout(i_dev, nodes=hier, out=lay)
-            ctx.notify_dispatch(i_dev, lay, handle=handle)
+        def upload(k):
+            sl = k % 2
+            with torch.cuda.stream(up):
+                up.wait_event(done[sl])
+                x_dev[sl].copy_(x_h, non_blocking=True)
+                i_dev[sl].copy_(i_h, non_blocking=True)
+                w_dev[sl].copy_(w_h, non_blocking=True)
+                in_ready[sl].record(up)
+
+        def compute(k):
+            sl = k % 2
+            stream.wait_event(in_ready[sl])
+            stream.wait_event(copied[sl])
+            ctx.get_dispatch_layout(i_dev[sl], nodes=hier, out=lay)
+            ctx.notify_dispatch(i_dev[sl], lay, handle=handle)
             if hier:
-                ctx.dispatch_hier(x_dev, i_dev, w_dev, handle, out=recv, staging=staging)
+                ctx.dispatch_hier(x_dev[sl], i_dev[sl], w_dev[sl], handle, out=recv, staging=staging)
             else:
-                ctx.dispatch(x_dev, i_dev, w_dev, handle, out=recv)
+                ctx.dispatch(x_dev[sl], i_dev[sl], w_dev[sl], handle, out=recv)
             ctx.permute(handle, recv, out=perm)
-            ctx.combine(handle, perm["permuted_x"], i_dev, w_dev, out=out, hier=hier)
-            out_h.copy_(out, non_blocking=True)
+            ctx.combine(handle, perm["permuted_x"], i_dev[sl], w_dev[sl], out=out_dev[sl], hier=hier)
+            done[sl].record(stream)
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
+        def download(k):
+            sl = k % 2
+            with torch.cuda.stream(down):
+                down.wait_event(done[sl])
+                out_h[sl].copy_(out_dev[sl], non_blocking=True)
+                copied[sl].record(down)
+
+        def run(nsteps):
+            upload(0)
+            for k in range(nsteps):
+                if k + 1 < nsteps:
+                    upload(k + 1)
+                compute(k)
+                download(k)
+            stream.wait_event(copied[(nsteps - 1) % 2])
+
+        run(max(2, args.warmup))
         torch.cuda.synchronize()
-        ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-        for i in range(args.steps):
-            flush.zero_()
-            ee[i][0].record(stream)
-            e2e_step()
-            ee[i][1].record(stream)
+        flush.zero_()
         torch.cuda.synchronize()
-        e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in ee) / args.steps)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run(args.steps)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ctx.check()
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+        # plain copy rates of this machine, for context
+        def rate(fn, nbytes):
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            fn()
+            a1.record(stream)
+            torch.cuda.synchronize()
+            return round(nbytes / a0.elapsed_time(a1) / 1e6, 1)
+        h2d_gbps = rate(lambda: x_dev[0].copy_(x_h, non_blocking=True), x.numel() * 2)
+        d2h_gbps = rate(lambda: out_h[0].copy_(out_dev[0], non_blocking=True), out.numel() * 2)
         h2d = x.numel() * 2 + topk_idx.numel() * 8 + topk_w.numel() * 4
         e2e = {"value": total_tokens / (e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": out.numel() * 2, "ms_per_step": round(e_ms, 4)}
+               "d2h_bytes_per_step": out.numel() * 2, "ms_per_step": round(e_ms, 4),
+               "pipelined": "inputs of step k+1 up and output of step k-1 down while step k computes",
+               "h2d_GBps": h2d_gbps, "d2h_GBps": d2h_gbps}
+        del x_dev, i_dev, w_dev, out_dev, out_h
 
     if rank != 0:
         epdist.shutdown()

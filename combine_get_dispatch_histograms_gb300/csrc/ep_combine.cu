@@ -206,7 +206,7 @@ ep_status launch_combine(const CombineArgs& a, int mode, int num_sms, cudaStream
     b.splits = splits;
     const int64_t items = n_tok * splits;
     int64_t want = (items + kCombineWarps - 1) / kCombineWarps;
-    const int64_t cap = (int64_t)num_sms * 3;
+    const int64_t cap = (int64_t)num_sms * 16;
     const int grid = (int)(want < cap ? want : cap);
     cudaError_t e = mode == 0 ? launch_mode<0>(b, grid, s) : mode == 1 ? launch_mode<1>(b, grid, s) : launch_mode<2>(b, grid, s);
     if (e != cudaSuccess) return cuda_error(e, "combine kernel");

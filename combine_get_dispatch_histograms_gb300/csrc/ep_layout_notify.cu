@@ -168,6 +168,32 @@ struct NotifyArgs {
     int32_t epoch;   // sequence number of this notify call
 };
 
+// Exclusive prefix sum over the block's threads (blockDim.x a multiple of 32,
+// at most 1024): warp shuffles, then the warp totals scanned by warp 0.
+__device__ int32_t block_exclusive_scan(int32_t v, int32_t* sh_tmp /* >= 32 ints */) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int32_t inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    __syncthreads();
+    if (lane == 31) sh_tmp[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t t = lane < nw ? sh_tmp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < nw) sh_tmp[lane] = t - (lane < nw ? sh_tmp[lane] : 0);  // exclusive warp offsets
+    }
+    __syncthreads();
+    return sh_tmp[warp] + inc - v;
+}
+
 __device__ void notify_global_scan(const NotifyArgs& a) {
     const int R = a.R, E = a.E, L = a.L, N = a.N, G = a.G;
     __shared__ int32_t sh_scan[kTileTokens];
@@ -211,18 +237,7 @@ __device__ void notify_global_scan(const NotifyArgs& a) {
     const int e0 = threadIdx.x * per;
     int32_t local = 0;
     for (int e = e0; e < e0 + per && e < E; ++e) local += a.h.num_recv_per_expert[e];
-    sh_scan[threadIdx.x] = local;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int32_t acc = 0;
-        for (int i = 0; i < (int)blockDim.x; ++i) {
-            const int32_t v = sh_scan[i];
-            sh_scan[i] = acc;
-            acc += v;
-        }
-    }
-    __syncthreads();
-    int32_t run = sh_scan[threadIdx.x];
+    int32_t run = block_exclusive_scan(local, sh_scan);
     for (int e = e0; e < e0 + per && e < E; ++e) {
         const int d = e / L;
         const int32_t c = a.h.num_recv_per_expert[e];

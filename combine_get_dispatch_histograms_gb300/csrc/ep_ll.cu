@@ -312,11 +312,13 @@ __device__ int wait_count(const int32_t* p, int64_t limit_ns, uint32_t* status) 
 }
 
 
-// grid = (R sources, E experts): CTA (s, e) waits for the counts of sources
-// 0..s of expert e (begin = exclusive prefix), then copies its messages.
+// grid = (R sources, E experts, Z): CTA (s, e, z) waits for the counts of
+// sources 0..s of expert e (begin = exclusive prefix), then copies its share
+// (every Z-th group of 4 messages) of region (e, s).
 __global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(LLRecvArgs a) {
     __shared__ int sh_begin, sh_count;
     const int s = blockIdx.x, e = blockIdx.y;
+    const int z = blockIdx.z, Z = gridDim.z;  // this CTA's share of the region's messages
     // launched as a programmatic dependent of the count publisher: start once
     // its grid (and every write before it) is complete
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(LLRecvArgs a) {
     __syncthreads();
     const int begin = sh_begin, count = sh_count;
     const int d = e / L, l = e % L;
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && z == 0) {
         int32_t* lr = a.layout_range + (((int64_t)d * L + l) * R + s) * 2;
         lr[0] = begin;
         lr[1] = count;
@@ -356,12 +358,15 @@ __global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(LLRecvArgs a) {
     const int64_t rows_per_expert = (int64_t)R * a.cap;
     const int nwarps = blockDim.x / 32;
     const int nv = H / 16;
-    for (int i = warp; i < count; i += nwarps) {
+    for (int i = z * nwarps + warp; i < count; i += nwarps * Z) {
         const uint8_t* msg = a.regions + (((int64_t)e * R + s) * a.cap + i) * a.msg_bytes;
         const int64_t p = ((int64_t)d * L + l) * rows_per_expert + begin + i;
         const int4* src = reinterpret_cast<const int4*>(msg + 16);
         int4* dx = reinterpret_cast<int4*>(a.packed_x + p * H);
-        // issue a batch of loads before the stores that consume them
+        // every load of the message (up to 16 vectors per lane) before the
+        // stores that consume them; the scales ride along
+        const float* sc = reinterpret_cast<const float*>(msg + 16 + H);
+        float scv = lane < S ? __ldcg(sc + lane) : 0.0f;
         for (int v0 = 0; v0 < nv; v0 += 8 * 32) {
             int4 buf[8];
 #pragma unroll
@@ -375,8 +380,8 @@ __global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(LLRecvArgs a) {
                 if (v < nv) __stcs(dx + v, buf[u]);
             }
         }
-        const float* sc = reinterpret_cast<const float*>(msg + 16 + H);
-        for (int v = lane; v < S; v += 32) __stcs(a.packed_scales + p * S + v, __ldcg(sc + v));
+        if (lane < S) __stcs(a.packed_scales + p * S + lane, scv);
+        for (int v = lane + 32; v < S; v += 32) __stcs(a.packed_scales + p * S + v, __ldcg(sc + v));
         if (lane == 0) {
             a.packed_src_info[p * 2] = s;
             a.packed_src_info[p * 2 + 1] = __ldcg(reinterpret_cast<const int32_t*>(msg));
@@ -575,7 +580,13 @@ extern "C" ep_status ep_ll_recv(ep_ll_buffer* b, uint8_t* packed_x, float* packe
     a.timeout_ns = b->wait_timeout_ns;
     a.status = b->status;
     cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(a.R, a.E);
+    // split a region's messages over Z CTAs when a full region is large (about
+    // 512 KB per CTA), so hot experts do not serialise on one CTA
+    int Z = (int)(((int64_t)b->cap * b->msg_bytes + (512 << 10) - 1) / (512 << 10));
+    if (const char* v = getenv("EP_LL_RECV_SPLIT")) Z = atoi(v);
+    if (Z < 1) Z = 1;
+    if (Z > 8) Z = 8;
+    lc.gridDim = dim3(a.R, a.E, Z);
     lc.blockDim = dim3(kRecvThreads);
     lc.dynamicSmemBytes = 0;
     lc.stream = as_stream(stream);
