@@ -35,13 +35,19 @@ def load_library():
 
 
 def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
-def _stream(stream) -> ctypes.c_void_p:
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream):
+    """cudaStream_t of `stream`, or of torch's current stream on the current device."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _require_cuda(*ts):
@@ -197,6 +203,19 @@ class Context:
             self._ctx, ctypes.byref(cs), _ptr(recv["recv_x"]), _ptr(recv["recv_src_rank"]),
             _ptr(recv["recv_src_idx"]), _ptr(recv["recv_topk_idx"]), handle.num_recv_rows,
             _ptr(o["permuted_x"]), _ptr(o["perm_src_row"]), o["permuted_x"].shape[0], _stream(stream)))
+        return o
+
+    def dispatch_permuted(self, x, topk_idx, topk_weights, handle: Handle, stream=None, out=None) -> dict:
+        """Fused dispatch: tokens straight into the expert-major layout."""
+        _require_cuda(x, topk_idx, topk_weights)
+        P = handle.num_perm_rows
+        o = out if out is not None else dict(
+            permuted_x=torch.empty(P, self.H, dtype=torch.bfloat16, device=self.device),
+            perm_src_token=self._i32(P), perm_weight=torch.empty(P, dtype=torch.float32, device=self.device))
+        cs = handle.c_struct()
+        check("ep_dispatch_permuted", self.lib.ep_dispatch_permuted(
+            self._ctx, _ptr(x), _ptr(topk_idx), _ptr(topk_weights), ctypes.byref(cs), _ptr(o["permuted_x"]),
+            _ptr(o["perm_src_token"]), _ptr(o.get("perm_weight")), o["permuted_x"].shape[0], _stream(stream)))
         return o
 
     # ---- combine ---------------------------------------------------------------

@@ -48,6 +48,7 @@ SIGNATURES = {
     "ep_notify_dispatch": (INT, [P, P, P, P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, P]),
     "ep_dispatch": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, P, P, I64, P]),
     "ep_permute": (INT, [P, ctypes.POINTER(EpDispatchHandle), P, P, P, P, I64, P, P, I64, P]),
+    "ep_dispatch_permuted": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, I64, P]),
     "ep_combine": (INT, [P, ctypes.POINTER(EpDispatchHandle), P, I64, P, P, P, P]),
     "ep_dispatch_hier": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, I64, P, P, P, P, P, I64, P]),
     "ep_combine_hier": (INT, [P, ctypes.POINTER(EpDispatchHandle), P, I64, P, P, P, P]),

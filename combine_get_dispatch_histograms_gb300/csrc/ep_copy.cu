@@ -6,6 +6,9 @@
 //  * local permute (page "事件驱动 EP 内核的调度策略与零拷贝通信", section "高吞吐量
 //    模式": received rows regrouped into contiguous per-expert blocks for the
 //    grouped GEMM);
+//  * fused dispatch (same pages, v2 direct mode's dispatch straight into the
+//    tensors the experts consume): each token written once per valid top-k
+//    entry into the expert-major layout, without the per-rank receive buffer;
 //  * hierarchical staging (page "DeepEP 学习笔记", section "hybrid 模式"; home
 //    rank rule from "零拷贝通信"): stage A one copy per destination node to the
 //    home rank, stage B forward inside the node.
@@ -101,6 +104,37 @@ struct PermuteRoute {
             return false;
         }
         perm_src_row[p] = (int32_t)u;
+        *row = p;
+        return true;
+    }
+};
+
+// fused dispatch: unit = source token g, candidates = its K top-k entries; the
+// row goes straight to its permuted rows (no receive buffer in between)
+struct PermutedScatterRoute {
+    const uint8_t* x;
+    uint8_t* permuted_x;
+    const int64_t* topk_idx;
+    const float* w;
+    const int32_t* perm_pos;
+    int32_t* perm_src_token;  // [P] s * T + t of each permuted row
+    float* perm_weight;       // [P] the entry's weight (nullable)
+    int K, E;
+    int64_t row_bytes;
+    int64_t perm_rows;
+    uint32_t* status;
+    __device__ const uint8_t* src(int64_t u) const { return x + u * row_bytes; }
+    __device__ uint8_t* dst(int64_t row) const { return permuted_x + row * row_bytes; }
+    __device__ bool candidate(int64_t u, int k, int64_t* row) const {
+        const int64_t e = topk_idx[u * K + k];
+        if (e < 0 || e >= E) return false;
+        const int32_t p = perm_pos[u * K + k];
+        if (p < 0 || p >= perm_rows) {
+            flag(status, FLAG_BOUNDS);
+            return false;
+        }
+        perm_src_token[p] = (int32_t)u;
+        if (perm_weight) perm_weight[p] = w[u * K + k];
         *row = p;
         return true;
     }
@@ -339,10 +373,15 @@ static EngineLaunch plan_engine(const ep_ctx* c, int64_t n_units, int64_t row_by
 }
 
 template <class Route, int DEPTH>
-static ep_status launch_depth(const Route& r, const EngineLaunch& p, cudaStream_t s, const char* what) {
-    cudaError_t e = cudaFuncSetAttribute(copy_engine_kernel<Route, DEPTH>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-    if (e != cudaSuccess) return cuda_error(e, what);
+static ep_status launch_depth(const Route& r, const EngineLaunch& p, int device, cudaStream_t s, const char* what) {
+    // the dynamic shared-memory limit is raised once per device and size
+    static int raised[kMaxDevicesTracked] = {};
+    if (device < 0 || device >= kMaxDevicesTracked || raised[device] < (int)p.smem) {
+        cudaError_t e = cudaFuncSetAttribute(copy_engine_kernel<Route, DEPTH>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+        if (e != cudaSuccess) return cuda_error(e, what);
+        if (device >= 0 && device < kMaxDevicesTracked) raised[device] = (int)p.smem;
+    }
     copy_engine_kernel<Route, DEPTH><<<p.grid, kCopyThreads, p.smem, s>>>(r, p.g);
     EP_CHECK_LAUNCH(what);
     return EP_OK;
@@ -351,12 +390,11 @@ static ep_status launch_depth(const Route& r, const EngineLaunch& p, cudaStream_
 template <class Route>
 static ep_status launch_engine(const ep_ctx* c, const Route& r, const EngineLaunch& p, cudaStream_t s,
                                const char* what) {
-    (void)c;
     if (p.g.n_units <= 0) return EP_OK;
     switch (p.depth) {
-        case 1: return launch_depth<Route, 1>(r, p, s, what);
-        case 2: return launch_depth<Route, 2>(r, p, s, what);
-        default: return launch_depth<Route, 3>(r, p, s, what);
+        case 1: return launch_depth<Route, 1>(r, p, c->device, s, what);
+        case 2: return launch_depth<Route, 2>(r, p, c->device, s, what);
+        default: return launch_depth<Route, 3>(r, p, c->device, s, what);
     }
 }
 
@@ -440,6 +478,40 @@ extern "C" ep_status ep_permute(ep_ctx* c, const ep_dispatch_handle* h, const vo
     r.status = c->status;
     EngineLaunch p = plan_engine(c, num_recv_rows, r.row_bytes, f.num_topk);
     st = launch_engine(c, r, p, as_stream(stream), "local permute");
+    if (st == EP_OK) c->last_launches = 1;
+    return st;
+}
+
+extern "C" ep_status ep_dispatch_permuted(ep_ctx* c, const void* x, const int64_t* topk_idx,
+                                          const float* topk_weights, const ep_dispatch_handle* h, void* permuted_x,
+                                          int32_t* perm_src_token, float* perm_weight, int64_t perm_capacity_rows,
+                                          void* stream) {
+    if (!c || !h) return set_error(EP_ERR_INVALID_ARG, "ctx or handle is NULL");
+    c->last_launches = 0;
+    const ep_config& f = c->cfg;
+    if (f.num_tokens == 0 || c->last_total_perm == 0) return EP_OK;
+    ep_status st;
+    if ((st = check_rows(x, "x")) != EP_OK || (st = check_rows(permuted_x, "permuted_x")) != EP_OK) return st;
+    if (!topk_idx || !h->perm_pos || !perm_src_token || (perm_weight && !topk_weights))
+        return set_error(EP_ERR_INVALID_ARG, "NULL fused dispatch argument");
+    if (perm_capacity_rows < c->last_total_perm)
+        return set_error(EP_ERR_CAPACITY, "permuted buffers hold %lld rows, notify counted %lld",
+                         (long long)perm_capacity_rows, (long long)c->last_total_perm);
+    PermutedScatterRoute r;
+    r.x = static_cast<const uint8_t*>(x);
+    r.permuted_x = static_cast<uint8_t*>(permuted_x);
+    r.topk_idx = topk_idx;
+    r.w = topk_weights;
+    r.perm_pos = h->perm_pos;
+    r.perm_src_token = perm_src_token;
+    r.perm_weight = perm_weight;
+    r.K = f.num_topk;
+    r.E = f.num_experts;
+    r.row_bytes = (int64_t)f.hidden * 2;
+    r.perm_rows = perm_capacity_rows;
+    r.status = c->status;
+    EngineLaunch p = plan_engine(c, (int64_t)f.num_ranks * f.num_tokens, r.row_bytes, f.num_topk);
+    st = launch_engine(c, r, p, as_stream(stream), "fused dispatch");
     if (st == EP_OK) c->last_launches = 1;
     return st;
 }

@@ -25,6 +25,7 @@ constexpr int kMaxTopk = 32;
 constexpr int kMaxLocalExperts = 1024;
 constexpr int kMaxExperts = 4096;
 constexpr int kTileTokens = 256;  // tokens per CTA of the layout / notify kernels
+constexpr int kMaxDevicesTracked = 64;  // per-device launch attributes cached up to this index
 
 // ---- host-side error plumbing -------------------------------------------------
 ep_status set_error(ep_status st, const char* fmt, ...);

@@ -194,11 +194,18 @@ __device__ int32_t block_exclusive_scan(int32_t v, int32_t* sh_tmp /* >= 32 ints
     return sh_tmp[warp] + inc - v;
 }
 
-__device__ void notify_global_scan(const NotifyArgs& a) {
+__device__ void notify_global_scan(const NotifyArgs& a, int32_t* sh /* >= 2E + 3R + 98 ints */) {
     const int R = a.R, E = a.E, L = a.L, N = a.N, G = a.G;
-    __shared__ int32_t sh_scan[kTileTokens];
-    __shared__ int32_t sh_total_recv;
-    // (a) transpose + exclusive prefix over sources, per receiver
+    int32_t* tot = sh;              // [E]  pairs per expert (over sources)
+    int32_t* off = tot + E;         // [E]  first permuted row of each expert
+    int32_t* nrecv = off + E;       // [R]  rows per receiver
+    int32_t* rbase = nrecv + R;     // [R+1]
+    int32_t* scan_tmp = rbase + R + 1;  // [32]
+    int32_t* hcnt = scan_tmp + 32;      // [R+1] staged rows per home rank
+    __shared__ int32_t sh_total_recv, sh_total_perm;
+    // (a) per receiver: the transpose of the count matrix and its exclusive
+    // prefix over sources; (b) per expert: totals over sources.  All loads of
+    // a thread are independent, so each phase costs one memory round trip.
     for (int d = threadIdx.x; d < R; d += blockDim.x) {
         int32_t acc = 0;
         for (int s = 0; s < R; ++s) {
@@ -209,74 +216,82 @@ __device__ void notify_global_scan(const NotifyArgs& a) {
         }
         a.h.num_recv_tokens[d] = acc;
         a.host[d] = acc;
+        nrecv[d] = acc;
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int32_t acc = 0;
+        for (int s = 0; s < R; ++s) acc += a.ntpe[(int64_t)s * E + e];
+        tot[e] = acc;
+        a.h.num_recv_per_expert[e] = acc;  // [d][l] flattened == e
+        a.host[R + e] = acc;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
         int32_t acc = 0;
         for (int d = 0; d < R; ++d) {
-            a.h.rank_base[d] = acc;
-            acc += a.h.num_recv_tokens[d];
+            rbase[d] = acc;
+            acc += nrecv[d];
         }
-        a.h.rank_base[R] = acc;
+        rbase[R] = acc;
         sh_total_recv = acc;
     }
-    // (b) per expert: counts over sources and the source-relative offsets
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int32_t run = 0;
-        for (int s = 0; s < R; ++s) {
-            a.ebase[(int64_t)s * E + e] = run;
-            run += a.ntpe[(int64_t)s * E + e];
-        }
-        a.h.num_recv_per_expert[e] = run;  // [d][l] flattened == e
-        a.host[R + e] = run;
-    }
-    __syncthreads();
-    // (c) exclusive scan over experts in (d, l) order: each thread owns a
-    // contiguous chunk, chunk sums are scanned in shared memory
+    // (c) exclusive scan over experts in (d, l) order: contiguous chunk per thread
     const int per = (E + blockDim.x - 1) / blockDim.x;
     const int e0 = threadIdx.x * per;
     int32_t local = 0;
-    for (int e = e0; e < e0 + per && e < E; ++e) local += a.h.num_recv_per_expert[e];
-    int32_t run = block_exclusive_scan(local, sh_scan);
+    for (int e = e0; e < e0 + per && e < E; ++e) local += tot[e];
+    int32_t run = block_exclusive_scan(local, scan_tmp);
     for (int e = e0; e < e0 + per && e < E; ++e) {
-        const int d = e / L;
-        const int32_t c = a.h.num_recv_per_expert[e];
-        // global first row of expert e, parked in expert_offsets for now
-        a.h.expert_offsets[e] = run;
-        if (e % L == 0) a.h.perm_rank_base[d] = run;
-        for (int s = 0; s < R; ++s) a.ebase[(int64_t)s * E + e] += run;
-        run += c;
-        if (e == E - 1) a.h.perm_rank_base[R] = run;
+        off[e] = run;
+        run += tot[e];
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) a.h.expert_offsets[e] -= a.h.perm_rank_base[e / L];
-    // (d) hierarchical staging bases: home rank h of node n = h / G receives
+    if (threadIdx.x == 0) sh_total_perm = off[E - 1] + tot[E - 1];
+    for (int d = threadIdx.x; d <= R; d += blockDim.x) {
+        a.h.rank_base[d] = rbase[d];
+        a.h.perm_rank_base[d] = d < R ? off[d * L] : off[E - 1] + tot[E - 1];
+    }
+    // (d) per expert: offsets inside the rank, and the first permuted row of
+    // every (source, expert) = the expert's first row + earlier sources' pairs
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int32_t o = off[e];
+        a.h.expert_offsets[e] = o - off[(e / L) * L];
+        int32_t acc = o;
+        for (int s = 0; s < R; ++s) {
+            a.ebase[(int64_t)s * E + e] = acc;
+            acc += a.ntpe[(int64_t)s * E + e];
+        }
+    }
+    // (e) hierarchical staging bases: home rank h of node n = h / G receives
     // from the sources s with s % G == h % G, in ascending s
     if (N > 1) {
         __syncthreads();
         for (int h = threadIdx.x; h < R; h += blockDim.x) {
             const int n = h / G;
             int32_t acc = 0;
-            for (int s = h % G; s < R; s += G) {
-                a.sbase[s * N + n] = acc;  // relative to stage_base[h]
-                acc += a.ntpn[s * N + n];
-            }
-            sh_scan[h] = acc;
+            for (int s = h % G; s < R; s += G) acc += a.ntpn[s * N + n];
+            hcnt[h] = acc;
         }
         __syncthreads();
         if (threadIdx.x == 0) {
             int32_t acc = 0;
             for (int h = 0; h < R; ++h) {
-                a.h.stage_base[h] = acc;
-                acc += sh_scan[h];
+                const int32_t c = hcnt[h];
+                hcnt[h] = acc;
+                acc += c;
             }
-            a.h.stage_base[R] = acc;
+            hcnt[R] = acc;
             a.host[R + E + 2] = acc;
         }
         __syncthreads();
+        for (int h = threadIdx.x; h <= R; h += blockDim.x) a.h.stage_base[h] = hcnt[h];
         for (int h = threadIdx.x; h < R; h += blockDim.x) {
             const int n = h / G;
-            for (int s = h % G; s < R; s += G) a.sbase[s * N + n] += a.h.stage_base[h];
+            int32_t acc = hcnt[h];
+            for (int s = h % G; s < R; s += G) {
+                a.sbase[s * N + n] = acc;
+                acc += a.ntpn[s * N + n];
+            }
         }
     } else if (threadIdx.x == 0) {
         a.host[R + E + 2] = 0;
@@ -284,7 +299,7 @@ __device__ void notify_global_scan(const NotifyArgs& a) {
     __syncthreads();
     if (threadIdx.x == 0) {
         a.host[R + E + 0] = sh_total_recv;
-        a.host[R + E + 1] = a.h.perm_rank_base[R];
+        a.host[R + E + 1] = sh_total_perm;
         a.host[R + E + 3] = (int32_t)atomicOr(a.status, 0u);
         __threadfence_system();
         // the host polls this word: it is written after every count above
@@ -295,11 +310,11 @@ __device__ void notify_global_scan(const NotifyArgs& a) {
 
 __global__ void __launch_bounds__(kTileTokens) notify_count_kernel(NotifyArgs a) {
     const int tiles = a.geom.tiles_per_src;
+    extern __shared__ int32_t sh_cnt[];  // [max(E + R + N, 2E + 3R + 98)]
     if ((int)blockIdx.x == a.R * tiles) {
-        notify_global_scan(a);
+        notify_global_scan(a, sh_cnt);
         return;
     }
-    extern __shared__ int32_t sh_cnt[];  // [E + R + N]
     const int s = blockIdx.x / tiles, tile = blockIdx.x % tiles;
     const int E = a.E, R = a.R, N = a.N, K = a.K, T = a.T;
     const int W = E + R + N;
@@ -744,7 +759,8 @@ extern "C" ep_status ep_notify_dispatch(ep_ctx* c, const int64_t* topk_idx, cons
     const int W = a.E + a.R + a.N;
     cudaStream_t s = as_stream(stream);
     const int nblk = a.R * c->tiles.tiles_per_src + 1;
-    notify_count_kernel<<<nblk, kTileTokens, sizeof(int32_t) * W, s>>>(a);
+    const int Wscan = 2 * a.E + 3 * a.R + 98;
+    notify_count_kernel<<<nblk, kTileTokens, sizeof(int32_t) * (W > Wscan ? W : Wscan), s>>>(a);
     EP_CHECK_LAUNCH("notify_count_kernel");
     EP_CUDA(cudaEventRecord(c->ev_counts, s));
     dim3 grid(c->tiles.tiles_per_src, a.R);

@@ -536,7 +536,11 @@ extern "C" ep_status ep_ll_send(ep_ll_buffer* b, const void* x, const int64_t* t
         const size_t smem = fixed + (size_t)stages * row_bytes;
         int64_t grid = (int64_t)b->num_sms * b->send_ctas_per_sm;
         if (grid > (int64_t)a.R * n) grid = (int64_t)a.R * n;
-        EP_CUDA(cudaFuncSetAttribute(ll_send_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        static int raised[kMaxDevicesTracked] = {};
+        if (b->device < 0 || b->device >= kMaxDevicesTracked || raised[b->device] < (int)smem) {
+            EP_CUDA(cudaFuncSetAttribute(ll_send_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+            if (b->device >= 0 && b->device < kMaxDevicesTracked) raised[b->device] = (int)smem;
+        }
         ll_send_kernel<<<(int)grid, 256, smem, s>>>(a, stages, 2000000000ll);
         EP_CHECK_LAUNCH("ll_send_kernel");
     }

@@ -217,6 +217,18 @@ ep_status ep_permute(ep_ctx* ctx, const ep_dispatch_handle* handle, const void* 
                      const int32_t* recv_topk_idx, int64_t num_recv_rows, void* permuted_x,
                      int32_t* perm_src_row, int64_t perm_capacity_rows, void* stream);
 
+/* Fused dispatch: each token written once per valid top-k entry straight into
+ * its permuted row (the expert-major blocks ep_permute produces), without the
+ * per-rank receive buffer ([P2] DeepEP v2 direct 模式: the dispatch kernel's
+ * epilogue arranges the data into the tensors the experts consume; this skips
+ * recv_x).  permuted_x [P][H] bf16 equals ep_permute's output;
+ * perm_src_token [P] int32 = s*T + t of each row; perm_weight [P] fp32
+ * (nullable) = the entry's weight.  Needs the handle of ep_notify_dispatch. */
+ep_status ep_dispatch_permuted(ep_ctx* ctx, const void* x, const int64_t* topk_idx,
+                               const float* topk_weights, const ep_dispatch_handle* handle,
+                               void* permuted_x, int32_t* perm_src_token, float* perm_weight,
+                               int64_t perm_capacity_rows, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Combine ([P2] combine 过程; v2 "rank-level partial result ... epilogue 按    */
 /* 不同 destination rank 做最终归约")                                             */

@@ -71,6 +71,20 @@ def compare_normal(R, E, K, T, H, C, x, idx, w, nodes=1, hier=False):
     eq(h["perm_pos"], o_perm["perm_pos"], "perm_pos")
     eq(perm["permuted_x"], o_perm["permuted_x"], "permuted_x")
     eq(perm["perm_src_row"], o_perm["perm_src_row"], "perm_src_row")
+    # fused dispatch straight into the permuted layout: the same rows
+    fused = ctx.dispatch_permuted(x.cuda(), idx.cuda(), w.cuda(), h)
+    ctx.check()
+    eq(fused["permuted_x"], o_perm["permuted_x"], "permuted_x (fused dispatch)")
+    pp = o_perm["perm_pos"]
+    P = int((pp >= 0).sum())
+    exp_tok = np.full(P, -1, np.int32)
+    exp_w = np.zeros(P, np.float32)
+    wn = w.numpy() if hasattr(w, "numpy") else np.asarray(w)
+    for s_, t_, k_ in zip(*np.nonzero(pp >= 0)):
+        exp_tok[pp[s_, t_, k_]] = s_ * T + t_
+        exp_w[pp[s_, t_, k_]] = wn[s_, t_, k_]
+    eq(fused["perm_src_token"], exp_tok, "perm_src_token")
+    eq(fused["perm_weight"], exp_w, "perm_weight")
     if hier:
         o_out = orc.combine_hier(o_perm["permuted_x"], o_perm["perm_pos"], idx, w, R, E, nodes)
     else:

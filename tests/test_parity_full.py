@@ -69,6 +69,13 @@ def _normal_full(wl, hier: bool):
     src_tok = o_disp["recv_src_rank"].astype(np.int64) * T + o_disp["recv_src_idx"]
     _rows_equal(recv["recv_x"], xf, src_tok, "recv_x")
     _rows_equal(perm["permuted_x"], xf, src_tok[o_perm["perm_src_row"]], "permuted_x")
+    if not hier:
+        del recv
+        fused = ctx.dispatch_permuted(x, idxd, wd, h)
+        ctx.check()
+        eq(fused["perm_src_token"], src_tok[o_perm["perm_src_row"]].astype(np.int32), "perm_src_token")
+        _rows_equal(fused["permuted_x"], xf, src_tok[o_perm["perm_src_row"]], "permuted_x (fused dispatch)")
+        del fused
     if hier:
         sb, sp = orc.hier_stage_pos(o_lay, R, T, N)
         eq(h["stage_base"], sb, "stage_base")
