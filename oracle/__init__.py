@@ -47,10 +47,13 @@ def build(force: bool = False) -> str:
 
 
 def lib():
+    """The oracle library.  EP_ORACLE_LIB names another build of ep_oracle.c
+    (the mutation tests load deliberately broken copies through it)."""
     global _lib
     with _lock:
         if _lib is None:
-            _lib = ctypes.CDLL(build())
+            path = os.environ.get("EP_ORACLE_LIB") or build()
+            _lib = ctypes.CDLL(path)
             _declare(_lib)
     return _lib
 

@@ -107,37 +107,53 @@ def test_hier_stage_positions(orc, T):
 
 
 def test_combine_exact_small(orc):
-    """ord32 against an exact-arithmetic restatement of the rank-partial order
-    (fp32 fma per rank, ranks summed ascending) on random tiny cases,
-    including cases where several experts of a token sit on one rank."""
+    """ord32 and the hierarchical order against an exact-arithmetic restatement
+    (fp32 fma per rank, ranks summed ascending; for the hierarchical order the
+    rank partials of a node summed first, then the nodes ascending) on random
+    tiny cases with 4 ranks and 2 nodes, values over a wide dynamic range so
+    that the order of three or more partials changes the rounding, including
+    tokens with several experts on one rank."""
     import torch
     rng = np.random.default_rng(3)
-    T, H = 2, 4
-    for trial in range(60):
-        idx = rng.integers(-1, E, size=(R, T, K)).astype(np.int64)
-        xw = rng.standard_normal((R, T, H)).astype(np.float32) * 3
+    R4, E4, K4, N4 = 4, 8, 4, 2
+    L4, G4 = E4 // R4, R4 // N4
+    T, H = 3, 8
+    for trial in range(40):
+        idx = rng.integers(-1, E4, size=(R4, T, K4)).astype(np.int64)
+        xw = (rng.standard_normal((R4, T, H)) * np.exp(rng.uniform(-6, 6, (R4, T, H)))).astype(np.float32)
         x = torch.from_numpy(xw).to(torch.bfloat16)
         xb = x.view(torch.int16).numpy().view(np.uint16)
-        w = rng.standard_normal((R, T, K)).astype(np.float32)
-        lay = orc.layout(idx, R, E)
-        note = orc.notify(lay, R, E, T, 2)
-        disp = orc.dispatch(x, idx, w, note, R, E)
-        perm = orc.permute(idx, disp["recv_x"], note, R, E)
-        out = orc.combine(perm["permuted_x"], perm["perm_pos"], idx, w, R, E, "ord32")
-        hout = orc.combine_hier(perm["permuted_x"], perm["perm_pos"], idx, w, R, E, 2)
-        for s in range(R):
+        w = (rng.standard_normal((R4, T, K4)) * np.exp(rng.uniform(-4, 4, (R4, T, K4)))).astype(np.float32)
+        lay = orc.layout(idx, R4, E4)
+        note = orc.notify(lay, R4, E4, T, 2)
+        disp = orc.dispatch(x, idx, w, note, R4, E4)
+        perm = orc.permute(idx, disp["recv_x"], note, R4, E4)
+        out = orc.combine(perm["permuted_x"], perm["perm_pos"], idx, w, R4, E4, "ord32")
+        hout = orc.combine_hier(perm["permuted_x"], perm["perm_pos"], idx, w, R4, E4, N4)
+        for s in range(R4):
             for t in range(T):
                 for j in range(H):
                     xv = pyref.bf16_value(xb[s, t, j])
-                    final = 0.0
-                    for d in range(R):
-                        ks = [k for k in range(K) if idx[s, t, k] >= 0 and idx[s, t, k] // L == d]
+                    partial = {}
+                    for d in range(R4):
+                        ks = [k for k in range(K4) if idx[s, t, k] >= 0 and idx[s, t, k] // L4 == d]
                         if not ks:
                             continue
                         p = 0.0
                         for k in ks:
                             p = pyref.fmaf(float(w[s, t, k]), xv, p)
-                        final = pyref.fadd(final, p)
+                        partial[d] = p
+                    final = 0.0
+                    for d in sorted(partial):
+                        final = pyref.fadd(final, partial[d])
                     assert out[s, t, j] == pyref.bf16_bits_of(final), (trial, s, t, j)
-                    # with one rank per node the node level adds nothing
-                    assert hout[s, t, j] == out[s, t, j]
+                    hfinal = 0.0
+                    for n in range(N4):
+                        ds = [d for d in sorted(partial) if d // G4 == n]
+                        if not ds:
+                            continue
+                        node = 0.0
+                        for d in ds:
+                            node = pyref.fadd(node, partial[d])
+                        hfinal = pyref.fadd(hfinal, node)
+                    assert hout[s, t, j] == pyref.bf16_bits_of(hfinal), (trial, s, t, j)
