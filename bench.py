@@ -385,6 +385,42 @@ def main():
                                        "frac": round(fb / (fd * 1e-3) / 1e9 / peak0, 3)}}
         del fperm
 
+    # ---- FP8 rows on the normal path: quantise once, then the fused dispatch ----
+    fp8 = None
+    if not hier and H % 128 == 0:
+        rq = ctx.fp8_row_bytes
+        xq = torch.empty(R * T, rq, dtype=torch.uint8, device="cuda")
+        fq = dict(permuted_xq=torch.empty(pairs, rq, dtype=torch.uint8, device="cuda"),
+                  perm_src_token=torch.empty(pairs, dtype=torch.int32, device="cuda"),
+                  perm_weight=torch.empty(pairs, dtype=torch.float32, device="cuda"))
+        for _ in range(args.warmup):
+            flush.zero_()
+            ctx.quantize_fp8(x, out=xq)
+            ctx.dispatch_permuted_fp8(xq, idx_d, w_d, handle, out=fq)
+        qt, dt = [], []
+        for i in range(args.steps):
+            flush.zero_()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record(stream)
+            ctx.quantize_fp8(x, out=xq)
+            e[1].record(stream)
+            ctx.dispatch_permuted_fp8(xq, idx_d, w_d, handle, out=fq)
+            e[2].record(stream)
+            torch.cuda.synchronize()
+            qt.append(e[0].elapsed_time(e[1]))
+            dt.append(e[1].elapsed_time(e[2]))
+        ctx.check()
+        peak0, _ = measured_hbm_gbs()
+        qb = tokens * (2 * H + rq)
+        db = (tokens + pairs) * rq
+        qm, dm = statistics.median(qt), statistics.median(dt)
+        fp8 = {"row_bytes": rq,
+               "quantize": {"us": round(qm * 1e3, 2), "algo_bytes": qb, "GBps": round(qb / qm / 1e6, 1),
+                            "frac": round(qb / qm / 1e6 / peak0, 3)},
+               "dispatch_permuted_fp8": {"us": round(dm * 1e3, 2), "algo_bytes": db, "GBps": round(db / dm / 1e6, 1),
+                                         "frac": round(db / dm / 1e6 / peak0, 3)}}
+        del xq, fq
+
     # ---- low-latency decode layer -------------------------------------------------
     ll = None
     if not args.no_ll:
@@ -609,6 +645,7 @@ def main():
         "wall_s_timed_region": round(wall, 4),
         "ll_decode": ll,
         "fused_path": fused,
+        "fp8_rows": fp8,
     }
     print(json.dumps(line), flush=True)
     epdist.shutdown()

@@ -218,6 +218,55 @@ class Context:
             _ptr(o["perm_src_token"]), _ptr(o.get("perm_weight")), o["permuted_x"].shape[0], _stream(stream)))
         return o
 
+    # ---- FP8 rows ----------------------------------------------------------------
+    @property
+    def fp8_row_bytes(self) -> int:
+        return int(self.lib.ep_fp8_row_bytes(self.H))
+
+    def quantize_fp8(self, x, stream=None, out=None):
+        """Every token once into an FP8 row (H e4m3 codes, H/128 fp32 scales)."""
+        _require_cuda(x)
+        o = out if out is not None else torch.empty(self.R * self.T, self.fp8_row_bytes, dtype=torch.uint8,
+                                                    device=self.device)
+        check("ep_quantize_fp8", self.lib.ep_quantize_fp8(self._ctx, _ptr(x), _ptr(o), _stream(stream)))
+        return o
+
+    def dispatch_fp8(self, xq, topk_idx, topk_weights, handle: Handle, stream=None, out=None) -> dict:
+        rows = handle.num_recv_rows
+        o = out if out is not None else dict(
+            recv_xq=torch.empty(rows, self.fp8_row_bytes, dtype=torch.uint8, device=self.device),
+            recv_src_rank=self._i32(rows), recv_src_idx=self._i32(rows), recv_topk_idx=self._i32(rows, self.K),
+            recv_topk_weights=torch.empty(rows, self.K, dtype=torch.float32, device=self.device))
+        cs = handle.c_struct()
+        check("ep_dispatch_fp8", self.lib.ep_dispatch_fp8(
+            self._ctx, _ptr(xq), _ptr(topk_idx), _ptr(topk_weights), ctypes.byref(cs), _ptr(o["recv_xq"]),
+            _ptr(o["recv_src_rank"]), _ptr(o["recv_src_idx"]), _ptr(o["recv_topk_idx"]),
+            _ptr(o["recv_topk_weights"]), o["recv_xq"].shape[0], _stream(stream)))
+        return o
+
+    def permute_fp8(self, handle: Handle, recv: dict, stream=None, out=None) -> dict:
+        P = handle.num_perm_rows
+        o = out if out is not None else dict(
+            permuted_xq=torch.empty(P, self.fp8_row_bytes, dtype=torch.uint8, device=self.device),
+            perm_src_row=self._i32(P))
+        cs = handle.c_struct()
+        check("ep_permute_fp8", self.lib.ep_permute_fp8(
+            self._ctx, ctypes.byref(cs), _ptr(recv["recv_xq"]), _ptr(recv["recv_src_rank"]),
+            _ptr(recv["recv_src_idx"]), _ptr(recv["recv_topk_idx"]), handle.num_recv_rows,
+            _ptr(o["permuted_xq"]), _ptr(o["perm_src_row"]), o["permuted_xq"].shape[0], _stream(stream)))
+        return o
+
+    def dispatch_permuted_fp8(self, xq, topk_idx, topk_weights, handle: Handle, stream=None, out=None) -> dict:
+        P = handle.num_perm_rows
+        o = out if out is not None else dict(
+            permuted_xq=torch.empty(P, self.fp8_row_bytes, dtype=torch.uint8, device=self.device),
+            perm_src_token=self._i32(P), perm_weight=torch.empty(P, dtype=torch.float32, device=self.device))
+        cs = handle.c_struct()
+        check("ep_dispatch_permuted_fp8", self.lib.ep_dispatch_permuted_fp8(
+            self._ctx, _ptr(xq), _ptr(topk_idx), _ptr(topk_weights), ctypes.byref(cs), _ptr(o["permuted_xq"]),
+            _ptr(o["perm_src_token"]), _ptr(o.get("perm_weight")), o["permuted_xq"].shape[0], _stream(stream)))
+        return o
+
     # ---- combine ---------------------------------------------------------------
     def combine(self, handle: Handle, expert_out, topk_idx, topk_weights, stream=None, out=None, hier=False):
         _require_cuda(expert_out, topk_idx, topk_weights)

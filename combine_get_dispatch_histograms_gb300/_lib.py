@@ -49,6 +49,11 @@ SIGNATURES = {
     "ep_dispatch": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, P, P, I64, P]),
     "ep_permute": (INT, [P, ctypes.POINTER(EpDispatchHandle), P, P, P, P, I64, P, P, I64, P]),
     "ep_dispatch_permuted": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, I64, P]),
+    "ep_fp8_row_bytes": (I64, [INT]),
+    "ep_quantize_fp8": (INT, [P, P, P, P]),
+    "ep_dispatch_fp8": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, P, P, I64, P]),
+    "ep_permute_fp8": (INT, [P, ctypes.POINTER(EpDispatchHandle), P, P, P, P, I64, P, P, I64, P]),
+    "ep_dispatch_permuted_fp8": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, I64, P]),
     "ep_combine": (INT, [P, ctypes.POINTER(EpDispatchHandle), P, I64, P, P, P, P]),
     "ep_dispatch_hier": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, I64, P, P, P, P, P, I64, P]),
     "ep_combine_hier": (INT, [P, ctypes.POINTER(EpDispatchHandle), P, I64, P, P, P, P]),

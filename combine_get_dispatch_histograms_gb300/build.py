@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libep_gb300.so")
-SOURCES = ["ep_layout_notify.cu", "ep_copy.cu", "ep_combine.cu", "ep_ll.cu"]
+SOURCES = ["ep_layout_notify.cu", "ep_copy.cu", "ep_combine.cu", "ep_ll.cu", "ep_fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

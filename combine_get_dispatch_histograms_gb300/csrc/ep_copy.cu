@@ -408,10 +408,11 @@ static ep_status check_rows(const void* p, const char* name) {
     return EP_OK;
 }
 
-extern "C" ep_status ep_dispatch(ep_ctx* c, const void* x, const int64_t* topk_idx, const float* topk_weights,
-                                 const ep_dispatch_handle* h, void* recv_x, int32_t* recv_src_rank,
-                                 int32_t* recv_src_idx, int32_t* recv_topk_idx, float* recv_topk_weights,
-                                 int64_t recv_capacity_rows, void* stream) {
+namespace ep {
+
+ep_status dispatch_rows(ep_ctx* c, const void* x, int64_t row_bytes, const int64_t* topk_idx, const float* topk_weights,
+                        const ep_dispatch_handle* h, void* recv_x, int32_t* recv_src_rank, int32_t* recv_src_idx,
+                        int32_t* recv_topk_idx, float* recv_topk_weights, int64_t recv_capacity_rows, void* stream) {
     if (!c || !h) return set_error(EP_ERR_INVALID_ARG, "ctx or handle is NULL");
     c->last_launches = 0;
     const ep_config& f = c->cfg;
@@ -439,17 +440,17 @@ extern "C" ep_status ep_dispatch(ep_ctx* c, const void* x, const int64_t* topk_i
     r.K = f.num_topk;
     r.T = f.num_tokens;
     r.L = c->L;
-    r.row_bytes = (int64_t)f.hidden * 2;
+    r.row_bytes = row_bytes;
     EngineLaunch p = plan_engine(c, (int64_t)f.num_ranks * f.num_tokens, r.row_bytes, f.num_ranks);
     st = launch_engine(c, r, p, as_stream(stream), "dispatch scatter");
     if (st == EP_OK) c->last_launches = 1;
     return st;
 }
 
-extern "C" ep_status ep_permute(ep_ctx* c, const ep_dispatch_handle* h, const void* recv_x,
-                                const int32_t* recv_src_rank, const int32_t* recv_src_idx,
-                                const int32_t* recv_topk_idx, int64_t num_recv_rows, void* permuted_x,
-                                int32_t* perm_src_row, int64_t perm_capacity_rows, void* stream) {
+ep_status permute_rows(ep_ctx* c, const ep_dispatch_handle* h, const void* recv_x, int64_t row_bytes,
+                       const int32_t* recv_src_rank, const int32_t* recv_src_idx, const int32_t* recv_topk_idx,
+                       int64_t num_recv_rows, void* permuted_x, int32_t* perm_src_row, int64_t perm_capacity_rows,
+                       void* stream) {
     if (!c || !h) return set_error(EP_ERR_INVALID_ARG, "ctx or handle is NULL");
     c->last_launches = 0;
     const ep_config& f = c->cfg;
@@ -473,7 +474,7 @@ extern "C" ep_status ep_permute(ep_ctx* c, const ep_dispatch_handle* h, const vo
     r.perm_src_row = perm_src_row;
     r.K = f.num_topk;
     r.T = f.num_tokens;
-    r.row_bytes = (int64_t)f.hidden * 2;
+    r.row_bytes = row_bytes;
     r.perm_rows = perm_capacity_rows;
     r.status = c->status;
     EngineLaunch p = plan_engine(c, num_recv_rows, r.row_bytes, f.num_topk);
@@ -482,10 +483,10 @@ extern "C" ep_status ep_permute(ep_ctx* c, const ep_dispatch_handle* h, const vo
     return st;
 }
 
-extern "C" ep_status ep_dispatch_permuted(ep_ctx* c, const void* x, const int64_t* topk_idx,
-                                          const float* topk_weights, const ep_dispatch_handle* h, void* permuted_x,
-                                          int32_t* perm_src_token, float* perm_weight, int64_t perm_capacity_rows,
-                                          void* stream) {
+ep_status dispatch_permuted_rows(ep_ctx* c, const void* x, int64_t row_bytes, const int64_t* topk_idx,
+                                 const float* topk_weights, const ep_dispatch_handle* h, void* permuted_x,
+                                 int32_t* perm_src_token, float* perm_weight, int64_t perm_capacity_rows,
+                                 void* stream) {
     if (!c || !h) return set_error(EP_ERR_INVALID_ARG, "ctx or handle is NULL");
     c->last_launches = 0;
     const ep_config& f = c->cfg;
@@ -507,13 +508,42 @@ extern "C" ep_status ep_dispatch_permuted(ep_ctx* c, const void* x, const int64_
     r.perm_weight = perm_weight;
     r.K = f.num_topk;
     r.E = f.num_experts;
-    r.row_bytes = (int64_t)f.hidden * 2;
+    r.row_bytes = row_bytes;
     r.perm_rows = perm_capacity_rows;
     r.status = c->status;
     EngineLaunch p = plan_engine(c, (int64_t)f.num_ranks * f.num_tokens, r.row_bytes, f.num_topk);
     st = launch_engine(c, r, p, as_stream(stream), "fused dispatch");
     if (st == EP_OK) c->last_launches = 1;
     return st;
+}
+
+}  // namespace ep
+
+extern "C" ep_status ep_dispatch(ep_ctx* c, const void* x, const int64_t* topk_idx, const float* topk_weights,
+                                 const ep_dispatch_handle* h, void* recv_x, int32_t* recv_src_rank,
+                                 int32_t* recv_src_idx, int32_t* recv_topk_idx, float* recv_topk_weights,
+                                 int64_t recv_capacity_rows, void* stream) {
+    if (!c) return set_error(EP_ERR_INVALID_ARG, "ctx is NULL");
+    return dispatch_rows(c, x, (int64_t)c->cfg.hidden * 2, topk_idx, topk_weights, h, recv_x, recv_src_rank,
+                         recv_src_idx, recv_topk_idx, recv_topk_weights, recv_capacity_rows, stream);
+}
+
+extern "C" ep_status ep_permute(ep_ctx* c, const ep_dispatch_handle* h, const void* recv_x,
+                                const int32_t* recv_src_rank, const int32_t* recv_src_idx,
+                                const int32_t* recv_topk_idx, int64_t num_recv_rows, void* permuted_x,
+                                int32_t* perm_src_row, int64_t perm_capacity_rows, void* stream) {
+    if (!c) return set_error(EP_ERR_INVALID_ARG, "ctx is NULL");
+    return permute_rows(c, h, recv_x, (int64_t)c->cfg.hidden * 2, recv_src_rank, recv_src_idx, recv_topk_idx,
+                        num_recv_rows, permuted_x, perm_src_row, perm_capacity_rows, stream);
+}
+
+extern "C" ep_status ep_dispatch_permuted(ep_ctx* c, const void* x, const int64_t* topk_idx,
+                                          const float* topk_weights, const ep_dispatch_handle* h, void* permuted_x,
+                                          int32_t* perm_src_token, float* perm_weight, int64_t perm_capacity_rows,
+                                          void* stream) {
+    if (!c) return set_error(EP_ERR_INVALID_ARG, "ctx is NULL");
+    return dispatch_permuted_rows(c, x, (int64_t)c->cfg.hidden * 2, topk_idx, topk_weights, h, permuted_x,
+                                  perm_src_token, perm_weight, perm_capacity_rows, stream);
 }
 
 extern "C" ep_status ep_dispatch_hier(ep_ctx* c, const void* x, const int64_t* topk_idx,

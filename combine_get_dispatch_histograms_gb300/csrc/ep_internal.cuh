@@ -207,6 +207,19 @@ __device__ __forceinline__ void bulk_wait_read() {
 }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// ---- row movers shared by the bf16 and fp8 entry points (ep_copy.cu) -------------
+ep_status dispatch_rows(ep_ctx* c, const void* x, int64_t row_bytes, const int64_t* topk_idx, const float* topk_weights,
+                        const ep_dispatch_handle* h, void* recv_x, int32_t* recv_src_rank, int32_t* recv_src_idx,
+                        int32_t* recv_topk_idx, float* recv_topk_weights, int64_t recv_capacity_rows, void* stream);
+ep_status permute_rows(ep_ctx* c, const ep_dispatch_handle* h, const void* recv_x, int64_t row_bytes,
+                       const int32_t* recv_src_rank, const int32_t* recv_src_idx, const int32_t* recv_topk_idx,
+                       int64_t num_recv_rows, void* permuted_x, int32_t* perm_src_row, int64_t perm_capacity_rows,
+                       void* stream);
+ep_status dispatch_permuted_rows(ep_ctx* c, const void* x, int64_t row_bytes, const int64_t* topk_idx,
+                                 const float* topk_weights, const ep_dispatch_handle* h, void* permuted_x,
+                                 int32_t* perm_src_token, float* perm_weight, int64_t perm_capacity_rows,
+                                 void* stream);
+
 // ---- launch helpers -------------------------------------------------------------
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 

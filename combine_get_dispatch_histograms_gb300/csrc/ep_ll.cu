@@ -25,6 +25,7 @@
 
 #include "ep_internal.cuh"
 #include "ep_combine.cuh"
+#include "ep_fp8.cuh"
 
 struct ep_ll_buffer {
     ep_config cfg;
@@ -59,10 +60,6 @@ struct LLSendArgs {
     uint32_t* status;
 };
 
-__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
-    // low byte <- a, high byte <- b
-    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-}
 
 // Persistent send: CTA c owns the contiguous tokens [q0, q1) of the flattened
 // (source, token) order.  Thread 0 streams their x rows global -> shared with
@@ -181,44 +178,15 @@ __global__ void __launch_bounds__(256) ll_send_kernel(LLSendArgs a, int stages, 
             if (act) {
                 const int4 p0 = *reinterpret_cast<const int4*>(xrow + (size_t)gi * 32);
                 const int4 p1 = *reinterpret_cast<const int4*>(xrow + (size_t)gi * 32 + 16);
-                const uint32_t uu[8] = {(uint32_t)p0.x, (uint32_t)p0.y, (uint32_t)p0.z, (uint32_t)p0.w,
-                                        (uint32_t)p1.x, (uint32_t)p1.y, (uint32_t)p1.z, (uint32_t)p1.w};
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    v[2 * u] = __uint_as_float(uu[u] << 16);
-                    v[2 * u + 1] = __uint_as_float(uu[u] & 0xffff0000u);
-                }
+                bf16x16_to_f32(p0, p1, v);
             } else {
 #pragma unroll
                 for (int u = 0; u < 16; ++u) v[u] = 0.0f;
             }
-            float amax = 0.0f;
-#pragma unroll
-            for (int u = 0; u < 16; ++u) amax = fmaxf(amax, fabsf(v[u]));
-            // max over the 8 lanes holding one 128-channel block
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const float scale = __fdiv_rn(amax, 448.0f);
-            uint32_t w4[4];
-            if (scale == 0.0f) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    uint32_t c = 0;
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) c |= ((__float_as_uint(v[4 * u + b]) >> 31) ? 0x80u : 0u) << (8 * b);
-                    w4[u] = c;
-                }
-            } else {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t lo = e4m3x2(__fdiv_rn(v[4 * u], scale), __fdiv_rn(v[4 * u + 1], scale));
-                    const uint32_t hi = e4m3x2(__fdiv_rn(v[4 * u + 2], scale), __fdiv_rn(v[4 * u + 3], scale));
-                    w4[u] = (lo & 0xffffu) | (hi << 16);
-                }
-            }
+            float scale;
+            const int4 codes = quantize16(v, &scale);
             if (act) {
-                *reinterpret_cast<int4*>(msg + 16 + (size_t)gi * 16) =
-                    make_int4((int)w4[0], (int)w4[1], (int)w4[2], (int)w4[3]);
+                *reinterpret_cast<int4*>(msg + 16 + (size_t)gi * 16) = codes;
                 if ((gi & 7) == 0) *reinterpret_cast<float*>(msg + 16 + H + (gi >> 3) * 4) = scale;
             }
         }

@@ -230,6 +230,36 @@ ep_status ep_dispatch_permuted(ep_ctx* ctx, const void* x, const int64_t* topk_i
                                int64_t perm_capacity_rows, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* FP8 rows for the normal path ([P2] 内存布局: a token's message carries x and  */
+/* its scales; [P1] 低延迟模式: hidden states travel as FP8, combine stays BF16) */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of one FP8 row: H e4m3 codes, then H/128 fp32 scales, padded to 16. */
+int64_t ep_fp8_row_bytes(int hidden);
+
+/* Quantises every token of x [R][T][H] bf16 once into xq [R*T][fp8 row]:
+ * per 128 channels scale = amax / 448 (fp32 division), code = e4m3
+ * RNE-satfinite of x / scale (fp32 division); a zero scale keeps only the
+ * sign.  Needs hidden % 128 == 0. */
+ep_status ep_quantize_fp8(ep_ctx* ctx, const void* x, uint8_t* xq, void* stream);
+
+/* ep_dispatch, ep_permute and ep_dispatch_permuted on FP8 rows (same metadata,
+ * same row positions; recv_xq / permuted_xq hold FP8 rows). */
+ep_status ep_dispatch_fp8(ep_ctx* ctx, const uint8_t* xq, const int64_t* topk_idx,
+                          const float* topk_weights, const ep_dispatch_handle* handle,
+                          uint8_t* recv_xq, int32_t* recv_src_rank, int32_t* recv_src_idx,
+                          int32_t* recv_topk_idx, float* recv_topk_weights,
+                          int64_t recv_capacity_rows, void* stream);
+ep_status ep_permute_fp8(ep_ctx* ctx, const ep_dispatch_handle* handle, const uint8_t* recv_xq,
+                         const int32_t* recv_src_rank, const int32_t* recv_src_idx,
+                         const int32_t* recv_topk_idx, int64_t num_recv_rows, uint8_t* permuted_xq,
+                         int32_t* perm_src_row, int64_t perm_capacity_rows, void* stream);
+ep_status ep_dispatch_permuted_fp8(ep_ctx* ctx, const uint8_t* xq, const int64_t* topk_idx,
+                                   const float* topk_weights, const ep_dispatch_handle* handle,
+                                   uint8_t* permuted_xq, int32_t* perm_src_token, float* perm_weight,
+                                   int64_t perm_capacity_rows, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Combine ([P2] combine 过程; v2 "rank-level partial result ... epilogue 按    */
 /* 不同 destination rank 做最终归约")                                             */
 /* ------------------------------------------------------------------------ */
