@@ -207,6 +207,42 @@ def oracle_parallel(workload, seconds: float):
                       f"{busy:.1f} s of oracle time per process ({wall:.1f} s wall incl. input generation)"}
 
 
+def run_ll_only(args):
+    """The decode low-latency layer alone (send, receive, combine), for a
+    profiler on a small case: prints the per-kernel times, not the contract line."""
+    import torch
+    from combine_get_dispatch_histograms_gb300 import LLBuffer, inputs
+    dw = inputs.WORKLOADS["decode"]
+    if args.ll_tokens:
+        dw = dw.replace(T=args.ll_tokens, ll_cap=args.ll_tokens)
+    idx, wt = inputs.make_routing(dw, 7)
+    x = inputs.make_x(dw, 7, device="cuda")
+    idxd, wd = idx.cuda(), wt.cuda()
+    buf = LLBuffer(dw.R, dw.E, dw.K, dw.T, dw.H, dw.ll_cap)
+    pk = buf.alloc_packed()
+    y = torch.zeros(pk["packed_x"].shape, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(dw.R, dw.T, dw.H, dtype=torch.bfloat16, device="cuda")
+    st = torch.cuda.current_stream()
+    times = []
+    for i in range(args.warmup + args.steps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(st)
+        buf.send(x, idxd, out=pk)
+        e[1].record(st)
+        buf.recv(pk)
+        e[2].record(st)
+        buf.combine(y, idxd, wd, pk, out=out)
+        e[3].record(st)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append([e[j].elapsed_time(e[j + 1]) * 1e3 for j in range(3)])
+    buf.check()
+    med = [statistics.median(t[j] for t in times) for j in range(3)] if times else [None] * 3
+    print(json.dumps({"ll_only": {"R": dw.R, "T": dw.T, "H": dw.H, "cap": dw.ll_cap,
+                                  "send_us": med[0], "recv_us": med[1], "combine_us": med[2]}}), flush=True)
+    return 0
+
+
 def run_reference(args, workload):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -246,6 +282,9 @@ def main():
     ap.add_argument("--workload", default="prefill", choices=["prefill", "skewed", "hier"])
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling on a smaller case)")
     ap.add_argument("--no-ll", action="store_true", help="skip the low-latency decode leg")
+    ap.add_argument("--ll-only", action="store_true",
+                    help="profiling mode: only the low-latency decode layer (no contract line)")
+    ap.add_argument("--ll-tokens", type=int, default=0, help="with --ll-only: T = cap of the decode layer")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -256,6 +295,8 @@ def main():
         workload = workload.replace(T=args.tokens)
     if args.impl == "reference":
         return run_reference(args, workload)
+    if args.ll_only:
+        return run_ll_only(args)
 
     import torch
     from combine_get_dispatch_histograms_gb300 import Context, LLBuffer
