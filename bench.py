@@ -426,6 +426,69 @@ def main():
                                        "frac": round(fb / (fd * 1e-3) / 1e9 / peak0, 3)}}
         del fperm
 
+    # ---- the same steps without a host synchronisation, replayed as one CUDA graph ----
+    # (notify's no-wait form; buffers sized for the worst case; the kernels read
+    # the row totals from the handle on the device)
+    nw_graph = None
+    if not hier:
+        rmax, pmax, _ = ctx.max_rows
+        g_recv = ctx.alloc_recv(rmax)
+        g_perm = dict(permuted_x=torch.empty(pmax, H, dtype=torch.bfloat16, device="cuda"),
+                      perm_src_row=torch.empty(pmax, dtype=torch.int32, device="cuda"))
+        g_fused = dict(permuted_x=g_perm["permuted_x"],
+                       perm_src_token=torch.empty(pmax, dtype=torch.int32, device="cuda"),
+                       perm_weight=torch.empty(pmax, dtype=torch.float32, device="cuda"))
+        g_out = torch.empty(R, T, H, dtype=torch.bfloat16, device="cuda")
+        g_lay = {k: torch.empty_like(v) for k, v in lay.items()}
+        g_h = ctx.alloc_handle()
+
+        def nw_step():
+            ctx.get_dispatch_layout(idx_d, out=g_lay)
+            ctx.notify_dispatch(idx_d, g_lay, handle=g_h, wait=False)
+            ctx.dispatch(x, idx_d, w_d, g_h, out=g_recv)
+            ctx.permute(g_h, g_recv, out=g_perm)
+            ctx.combine(g_h, g_perm["permuted_x"], idx_d, w_d, out=g_out)
+
+        def nw_fused():
+            ctx.get_dispatch_layout(idx_d, out=g_lay)
+            ctx.notify_dispatch(idx_d, g_lay, handle=g_h, wait=False)
+            ctx.dispatch_permuted(x, idx_d, w_d, g_h, out=g_fused)
+            ctx.combine(g_h, g_fused["permuted_x"], idx_d, w_d, out=g_out)
+
+        nw_graph = {"steps": "one CUDA graph per step: layout -> notify (no host wait) -> ... ; "
+                          "worst-case buffers, row totals read on the device"}
+        for name, fn in (("step", nw_step), ("fused_path", nw_fused)):
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                fn()  # eager once outside the capture
+            stream.wait_stream(side)
+            torch.cuda.synchronize()
+            cg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(cg):
+                fn()
+            for _ in range(args.warmup):
+                flush.zero_()
+                cg.replay()
+            gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+            for i in range(args.steps):
+                flush.zero_()
+                gev[i][0].record(stream)
+                cg.replay()
+                gev[i][1].record(stream)
+            torch.cuda.synchronize()
+            ctx.check()
+            # the replayed step gives the eager step's output, bit for bit
+            step()
+            torch.cuda.synchronize()
+            if not torch.equal(g_out.view(torch.int16), out.view(torch.int16)):
+                raise RuntimeError(f"graph {name}: output differs from the eager step")
+            gms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in gev) / args.steps)
+            nw_graph[name] = {"ms_per_step": round(gms, 4),
+                           "tokens_per_s": round(sum_over_ranks(tokens) / (gms / 1e3), 1)}
+            del cg
+        del g_recv, g_perm, g_fused, g_out
+
     # ---- FP8 rows on the normal path: quantise once, then the fused dispatch ----
     fp8 = None
     if not hier and H % 128 == 0:
@@ -686,6 +749,7 @@ def main():
         "wall_s_timed_region": round(wall, 4),
         "ll_decode": ll,
         "fused_path": fused,
+        "graph": nw_graph,
         "fp8_rows": fp8,
     }
     print(json.dumps(line), flush=True)

@@ -160,21 +160,45 @@ class Context:
             h["stage_pos"] = self._i32(R, T, N)
         return h
 
-    def notify_dispatch(self, topk_idx: torch.Tensor, layout: dict, stream=None, handle: Optional[Handle] = None) -> Handle:
+    @property
+    def max_rows(self) -> tuple:
+        """Worst-case (received, permuted, staged) row counts: buffers of these
+        sizes never overflow, whatever the routing."""
+        R, T, K, N = self.R, self.T, self.K, self.N
+        return R * T * min(K, R), R * T * K, (R * T * min(K, N) if N > 1 else 0)
+
+    def notify_dispatch(self, topk_idx: torch.Tensor, layout: dict, stream=None, handle: Optional[Handle] = None,
+                        wait: bool = True) -> Handle:
+        """wait=False: no host synchronisation (graph-capturable).  The row
+        totals then stay on the device (handle["rank_base"][R], ["perm_rank_base"][R],
+        ["stage_base"][R]) and the handle's num_*_rows are the worst-case bounds."""
         _require_cuda(topk_idx)
         h = handle if handle is not None else self.alloc_handle()
-        host_recv, host_exp, host_tot = self._host_recv, self._host_exp, self._host_tot
         cs = h.c_struct()
+        if wait:
+            host_recv, host_exp, host_tot = self._host_recv, self._host_exp, self._host_tot
+        else:
+            host_recv = host_exp = host_tot = None
         check("ep_notify_dispatch", self.lib.ep_notify_dispatch(
             self._ctx, _ptr(topk_idx), _ptr(layout["num_tokens_per_expert"]), _ptr(layout["num_tokens_per_rank"]),
             _ptr(layout["is_token_in_rank"]), _ptr(layout.get("num_tokens_per_node")),
             _ptr(layout.get("is_token_in_node")), ctypes.byref(cs), host_recv, host_exp, host_tot, _stream(stream)))
-        h.host_num_recv_tokens = list(host_recv)
-        h.host_num_recv_per_expert = list(host_exp)
-        h.num_recv_rows, h.num_perm_rows, h.num_stage_rows = (int(v) for v in host_tot)
+        h.synced = wait
+        if wait:
+            h.host_num_recv_tokens = list(host_recv)
+            h.host_num_recv_per_expert = list(host_exp)
+            h.num_recv_rows, h.num_perm_rows, h.num_stage_rows = (int(v) for v in host_tot)
+        else:
+            h.host_num_recv_tokens = h.host_num_recv_per_expert = None
+            h.num_recv_rows, h.num_perm_rows, h.num_stage_rows = self.max_rows
         return h
 
     # ---- dispatch / permute ----------------------------------------------------
+    @staticmethod
+    def _recv_rows(handle: Handle, recv_rows: torch.Tensor) -> int:
+        # rows permute may read: the waited total, else the recv buffer's capacity
+        return handle.num_recv_rows if getattr(handle, "synced", True) else recv_rows.shape[0]
+
     def alloc_recv(self, rows: int) -> dict:
         return dict(
             recv_x=torch.empty(rows, self.H, dtype=torch.bfloat16, device=self.device),
@@ -201,7 +225,7 @@ class Context:
         cs = handle.c_struct()
         check("ep_permute", self.lib.ep_permute(
             self._ctx, ctypes.byref(cs), _ptr(recv["recv_x"]), _ptr(recv["recv_src_rank"]),
-            _ptr(recv["recv_src_idx"]), _ptr(recv["recv_topk_idx"]), handle.num_recv_rows,
+            _ptr(recv["recv_src_idx"]), _ptr(recv["recv_topk_idx"]), self._recv_rows(handle, recv["recv_x"]),
             _ptr(o["permuted_x"]), _ptr(o["perm_src_row"]), o["permuted_x"].shape[0], _stream(stream)))
         return o
 
@@ -252,7 +276,7 @@ class Context:
         cs = handle.c_struct()
         check("ep_permute_fp8", self.lib.ep_permute_fp8(
             self._ctx, ctypes.byref(cs), _ptr(recv["recv_xq"]), _ptr(recv["recv_src_rank"]),
-            _ptr(recv["recv_src_idx"]), _ptr(recv["recv_topk_idx"]), handle.num_recv_rows,
+            _ptr(recv["recv_src_idx"]), _ptr(recv["recv_topk_idx"]), self._recv_rows(handle, recv["recv_xq"]),
             _ptr(o["permuted_xq"]), _ptr(o["perm_src_row"]), o["permuted_xq"].shape[0], _stream(stream)))
         return o
 

@@ -34,7 +34,8 @@ constexpr int kBatch = 32;      // units per table batch
 constexpr int kMaxStages = 16;
 
 struct CopyGeom {
-    int64_t n_units;
+    int64_t n_units;               // units, or the most units when n_units_dev is given
+    const int32_t* n_units_dev;    // nullable: actual count on the device (clamped to n_units)
     int64_t row_bytes;
     int32_t chunk_bytes;
     int32_t nchunks;
@@ -60,12 +61,18 @@ struct ScatterRoute {
     float* recv_topk_w;
     int R, K, T, L;
     int64_t row_bytes;
+    int64_t recv_rows;  // rows the recv buffers hold
+    uint32_t* status;
     __device__ const uint8_t* src(int64_t u) const { return x + u * row_bytes; }
     __device__ uint8_t* dst(int64_t row) const { return recv_x + row * row_bytes; }
     __device__ bool candidate(int64_t u, int d, int64_t* row) const {
         const int32_t sp = send_pos[u * R + d];
         if (sp < 0) return false;
         const int64_t r = (int64_t)rank_base[d] + sp;
+        if (r >= recv_rows) {  // more rows than the caller's buffers hold
+            flag(status, FLAG_CAPACITY);
+            return false;
+        }
         *row = r;
         const int s = (int)(u / T), t = (int)(u % T);
         recv_src_rank[r] = s;
@@ -100,7 +107,7 @@ struct PermuteRoute {
         const int64_t g = (int64_t)recv_src_rank[u] * T + recv_src_idx[u];
         const int32_t p = perm_pos[g * K + k];
         if (p < 0 || p >= perm_rows) {
-            flag(status, FLAG_BOUNDS);
+            flag(status, p < 0 ? FLAG_BOUNDS : FLAG_CAPACITY);
             return false;
         }
         perm_src_row[p] = (int32_t)u;
@@ -130,7 +137,7 @@ struct PermutedScatterRoute {
         if (e < 0 || e >= E) return false;
         const int32_t p = perm_pos[u * K + k];
         if (p < 0 || p >= perm_rows) {
-            flag(status, FLAG_BOUNDS);
+            flag(status, p < 0 ? FLAG_BOUNDS : FLAG_CAPACITY);
             return false;
         }
         perm_src_token[p] = (int32_t)u;
@@ -149,11 +156,17 @@ struct StageARoute {
     int32_t* stage_src_idx;
     int N, T;
     int64_t row_bytes;
+    int64_t stage_rows;  // rows the staging buffers hold
+    uint32_t* status;
     __device__ const uint8_t* src(int64_t u) const { return x + u * row_bytes; }
     __device__ uint8_t* dst(int64_t row) const { return staging + row * row_bytes; }
     __device__ bool candidate(int64_t u, int n, int64_t* row) const {
         const int32_t p = stage_pos[u * N + n];
         if (p < 0) return false;
+        if (p >= stage_rows) {
+            flag(status, FLAG_CAPACITY);
+            return false;
+        }
         stage_src_rank[p] = (int32_t)(u / T);
         stage_src_idx[p] = (int32_t)(u % T);
         *row = p;
@@ -178,6 +191,8 @@ struct StageBRoute {
     float* recv_topk_w;
     int R, K, T, L, G;
     int64_t row_bytes;
+    int64_t recv_rows;
+    uint32_t* status;
     __device__ const uint8_t* src(int64_t u) const { return staging + u * row_bytes; }
     __device__ uint8_t* dst(int64_t row) const { return recv_x + row * row_bytes; }
     __device__ bool candidate(int64_t u, int j, int64_t* row) const {
@@ -195,6 +210,10 @@ struct StageBRoute {
         const int32_t sp = send_pos[g * R + d];
         if (sp < 0) return false;
         const int64_t r = (int64_t)rank_base[d] + sp;
+        if (r >= recv_rows) {
+            flag(status, FLAG_CAPACITY);
+            return false;
+        }
         *row = r;
         recv_src_rank[r] = s;
         recv_src_idx[r] = t;
@@ -253,8 +272,14 @@ __global__ void __launch_bounds__(kCopyThreads) copy_engine_kernel(Route route, 
     sm.rows = reinterpret_cast<int64_t*>(smem_raw + kMaxStages * sizeof(uint64_t) + 2 * kBatch * sizeof(int32_t));
     sm.stage = smem_raw + engine_stage_offset(g.fanout);
 
-    const int64_t u_begin = g.n_units * blockIdx.x / gridDim.x;
-    const int64_t u_end = g.n_units * (blockIdx.x + 1) / gridDim.x;
+    int64_t total = g.n_units;
+    if (g.n_units_dev) {
+        const int64_t dv = *g.n_units_dev;
+        if (dv > total && threadIdx.x == 0 && blockIdx.x == 0) flag(g.status, FLAG_CAPACITY);
+        total = dv < total ? (dv > 0 ? dv : 0) : total;
+    }
+    const int64_t u_begin = total * blockIdx.x / gridDim.x;
+    const int64_t u_end = total * (blockIdx.x + 1) / gridDim.x;
     const int64_t n_units = u_end - u_begin;
     const int nbatches = (int)((n_units + kBatch - 1) / kBatch);
     const int64_t J = n_units * g.nchunks;  // jobs of this CTA
@@ -347,6 +372,7 @@ struct EngineLaunch {
 static EngineLaunch plan_engine(const ep_ctx* c, int64_t n_units, int64_t row_bytes, int fanout) {
     EngineLaunch p;
     p.g.n_units = n_units;
+    p.g.n_units_dev = nullptr;
     p.g.row_bytes = row_bytes;
     p.g.fanout = fanout;
     p.g.timeout_ns = c->wait_timeout_ns;
@@ -416,13 +442,13 @@ ep_status dispatch_rows(ep_ctx* c, const void* x, int64_t row_bytes, const int64
     if (!c || !h) return set_error(EP_ERR_INVALID_ARG, "ctx or handle is NULL");
     c->last_launches = 0;
     const ep_config& f = c->cfg;
-    if (f.num_tokens == 0 || c->last_total_recv == 0) return EP_OK;
+    if (f.num_tokens == 0 || (c->totals_known && c->last_total_recv == 0) || recv_capacity_rows == 0) return EP_OK;
     ep_status st;
     if ((st = check_rows(x, "x")) != EP_OK || (st = check_rows(recv_x, "recv_x")) != EP_OK) return st;
     if (!topk_idx || !topk_weights || !h->send_pos || !h->rank_base || !recv_src_rank || !recv_src_idx ||
         !recv_topk_idx || !recv_topk_weights)
         return set_error(EP_ERR_INVALID_ARG, "NULL dispatch argument");
-    if (recv_capacity_rows < c->last_total_recv)
+    if (c->totals_known && recv_capacity_rows < c->last_total_recv)
         return set_error(EP_ERR_CAPACITY, "recv buffers hold %lld rows, notify counted %lld",
                          (long long)recv_capacity_rows, (long long)c->last_total_recv);
     ScatterRoute r;
@@ -441,6 +467,8 @@ ep_status dispatch_rows(ep_ctx* c, const void* x, int64_t row_bytes, const int64
     r.T = f.num_tokens;
     r.L = c->L;
     r.row_bytes = row_bytes;
+    r.recv_rows = recv_capacity_rows;
+    r.status = c->status;
     EngineLaunch p = plan_engine(c, (int64_t)f.num_ranks * f.num_tokens, r.row_bytes, f.num_ranks);
     st = launch_engine(c, r, p, as_stream(stream), "dispatch scatter");
     if (st == EP_OK) c->last_launches = 1;
@@ -455,13 +483,13 @@ ep_status permute_rows(ep_ctx* c, const ep_dispatch_handle* h, const void* recv_
     c->last_launches = 0;
     const ep_config& f = c->cfg;
     if (num_recv_rows < 0) return set_error(EP_ERR_INVALID_ARG, "num_recv_rows < 0");
-    if (num_recv_rows == 0) return EP_OK;
+    if (num_recv_rows == 0 || (c->totals_known && c->last_total_recv == 0)) return EP_OK;
     ep_status st;
     if ((st = check_rows(recv_x, "recv_x")) != EP_OK || (st = check_rows(permuted_x, "permuted_x")) != EP_OK)
         return st;
-    if (!recv_src_rank || !recv_src_idx || !recv_topk_idx || !perm_src_row || !h->perm_pos)
+    if (!recv_src_rank || !recv_src_idx || !recv_topk_idx || !perm_src_row || !h->perm_pos || !h->rank_base)
         return set_error(EP_ERR_INVALID_ARG, "NULL permute argument");
-    if (perm_capacity_rows < c->last_total_perm)
+    if (c->totals_known && perm_capacity_rows < c->last_total_perm)
         return set_error(EP_ERR_CAPACITY, "permuted buffers hold %lld rows, notify counted %lld",
                          (long long)perm_capacity_rows, (long long)c->last_total_perm);
     PermuteRoute r;
@@ -478,6 +506,7 @@ ep_status permute_rows(ep_ctx* c, const ep_dispatch_handle* h, const void* recv_
     r.perm_rows = perm_capacity_rows;
     r.status = c->status;
     EngineLaunch p = plan_engine(c, num_recv_rows, r.row_bytes, f.num_topk);
+    p.g.n_units_dev = h->rank_base + f.num_ranks;  // rows actually received, at most num_recv_rows
     st = launch_engine(c, r, p, as_stream(stream), "local permute");
     if (st == EP_OK) c->last_launches = 1;
     return st;
@@ -490,12 +519,12 @@ ep_status dispatch_permuted_rows(ep_ctx* c, const void* x, int64_t row_bytes, co
     if (!c || !h) return set_error(EP_ERR_INVALID_ARG, "ctx or handle is NULL");
     c->last_launches = 0;
     const ep_config& f = c->cfg;
-    if (f.num_tokens == 0 || c->last_total_perm == 0) return EP_OK;
+    if (f.num_tokens == 0 || (c->totals_known && c->last_total_perm == 0) || perm_capacity_rows == 0) return EP_OK;
     ep_status st;
     if ((st = check_rows(x, "x")) != EP_OK || (st = check_rows(permuted_x, "permuted_x")) != EP_OK) return st;
     if (!topk_idx || !h->perm_pos || !perm_src_token || (perm_weight && !topk_weights))
         return set_error(EP_ERR_INVALID_ARG, "NULL fused dispatch argument");
-    if (perm_capacity_rows < c->last_total_perm)
+    if (c->totals_known && perm_capacity_rows < c->last_total_perm)
         return set_error(EP_ERR_CAPACITY, "permuted buffers hold %lld rows, notify counted %lld",
                          (long long)perm_capacity_rows, (long long)c->last_total_perm);
     PermutedScatterRoute r;
@@ -556,7 +585,9 @@ extern "C" ep_status ep_dispatch_hier(ep_ctx* c, const void* x, const int64_t* t
     c->last_launches = 0;
     const ep_config& f = c->cfg;
     if (f.num_nodes < 2) return set_error(EP_ERR_INVALID_ARG, "ep_dispatch_hier needs num_nodes > 1");
-    if (f.num_tokens == 0 || c->last_total_recv == 0) return EP_OK;
+    if (f.num_tokens == 0 || (c->totals_known && c->last_total_recv == 0) || recv_capacity_rows == 0 ||
+        stage_capacity_rows == 0)
+        return EP_OK;
     ep_status st;
     if ((st = check_rows(x, "x")) != EP_OK || (st = check_rows(recv_x, "recv_x")) != EP_OK ||
         (st = check_rows(staging, "staging")) != EP_OK)
@@ -565,7 +596,7 @@ extern "C" ep_status ep_dispatch_hier(ep_ctx* c, const void* x, const int64_t* t
         !stage_src_rank || !stage_src_idx || !recv_src_rank || !recv_src_idx || !recv_topk_idx ||
         !recv_topk_weights)
         return set_error(EP_ERR_INVALID_ARG, "NULL hierarchical dispatch argument");
-    if (stage_capacity_rows < c->last_total_stage || recv_capacity_rows < c->last_total_recv)
+    if (c->totals_known && (stage_capacity_rows < c->last_total_stage || recv_capacity_rows < c->last_total_recv))
         return set_error(EP_ERR_CAPACITY, "staging / recv buffers smaller than notify's counts");
     const int64_t row_bytes = (int64_t)f.hidden * 2;
     StageARoute a;
@@ -577,6 +608,8 @@ extern "C" ep_status ep_dispatch_hier(ep_ctx* c, const void* x, const int64_t* t
     a.N = f.num_nodes;
     a.T = f.num_tokens;
     a.row_bytes = row_bytes;
+    a.stage_rows = stage_capacity_rows;
+    a.status = c->status;
     EngineLaunch pa = plan_engine(c, (int64_t)f.num_ranks * f.num_tokens, row_bytes, f.num_nodes);
     st = launch_engine(c, a, pa, as_stream(stream), "hierarchical stage A");
     if (st != EP_OK) return st;
@@ -600,7 +633,10 @@ extern "C" ep_status ep_dispatch_hier(ep_ctx* c, const void* x, const int64_t* t
     b.L = c->L;
     b.G = c->G;
     b.row_bytes = row_bytes;
-    EngineLaunch pb = plan_engine(c, c->last_total_stage, row_bytes, c->G);
+    b.recv_rows = recv_capacity_rows;
+    b.status = c->status;
+    EngineLaunch pb = plan_engine(c, c->totals_known ? c->last_total_stage : stage_capacity_rows, row_bytes, c->G);
+    pb.g.n_units_dev = h->stage_base + f.num_ranks;  // rows actually staged
     st = launch_engine(c, b, pb, as_stream(stream), "hierarchical stage B");
     if (st == EP_OK) c->last_launches = 2;
     return st;

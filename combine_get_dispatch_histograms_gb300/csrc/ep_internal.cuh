@@ -101,6 +101,7 @@ struct ep_ctx {
     int copy_ctas_per_sm, copy_stage_bytes, copy_read_depth;
     // totals of the last notify (host copies), sizes of later launches
     int64_t last_total_recv, last_total_perm, last_total_stage;
+    bool totals_known;  // false after a notify that did not wait for the counts
     int last_launches;
 };
 

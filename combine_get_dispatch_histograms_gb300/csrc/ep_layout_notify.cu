@@ -546,6 +546,7 @@ extern "C" ep_status ep_ctx_create(const ep_config* cfg, ep_ctx** out) {
     ep_status st = validate_config(cfg);
     if (st != EP_OK) return st;
     ep_ctx* c = new ep_ctx();
+    c->totals_known = true;  // nothing notified yet: zero rows
     std::memset(c, 0, sizeof(*c));
     c->cfg = *cfg;
     c->L = cfg->num_experts / cfg->num_ranks;
@@ -726,8 +727,11 @@ extern "C" ep_status ep_notify_dispatch(ep_ctx* c, const int64_t* topk_idx, cons
     c->last_launches = 0;
     const ep_config& f = c->cfg;
     const bool hier = f.num_nodes > 1;
-    if (!ntpe || !ntpr || !host_num_recv || (f.num_tokens > 0 && (!itir || !topk_idx)))
+    if (!ntpe || !ntpr || (f.num_tokens > 0 && (!itir || !topk_idx)))
         return set_error(EP_ERR_INVALID_ARG, "NULL notify input");
+    const bool wait = host_num_recv != nullptr;
+    if (!wait && (host_num_recv_per_expert || host_totals))
+        return set_error(EP_ERR_INVALID_ARG, "host count arrays need host_num_recv_tokens (the waiting form)");
     if (hier && (!ntpn || !h->stage_base || (f.num_tokens > 0 && (!itin || !h->stage_pos))))
         return set_error(EP_ERR_INVALID_ARG, "hierarchical mode needs node layout and stage_* handle arrays");
     if (!h->recv_count || !h->recv_offsets || !h->num_recv_tokens || !h->rank_base || !h->num_recv_per_expert ||
@@ -762,11 +766,17 @@ extern "C" ep_status ep_notify_dispatch(ep_ctx* c, const int64_t* topk_idx, cons
     const int Wscan = 2 * a.E + 3 * a.R + 98;
     notify_count_kernel<<<nblk, kTileTokens, sizeof(int32_t) * (W > Wscan ? W : Wscan), s>>>(a);
     EP_CHECK_LAUNCH("notify_count_kernel");
-    EP_CUDA(cudaEventRecord(c->ev_counts, s));
+    if (wait) EP_CUDA(cudaEventRecord(c->ev_counts, s));
     dim3 grid(c->tiles.tiles_per_src, a.R);
     notify_position_kernel<<<grid, kTileTokens, notify_position_smem(c), s>>>(a);
     EP_CHECK_LAUNCH("notify_position_kernel");
     c->last_launches = 2;
+    if (!wait) {
+        // no host synchronisation: later calls size their grids from their
+        // capacity arguments and read the row counts from the handle on the device
+        c->totals_known = false;
+        return EP_OK;
+    }
     // the one host synchronisation of the normal path: the receive counts.
     // Poll the CPU-mapped sequence word the count kernel writes last (cheaper
     // than an event wake-up); the event bounds the poll and reports errors.
@@ -797,6 +807,7 @@ extern "C" ep_status ep_notify_dispatch(ep_ctx* c, const int64_t* topk_idx, cons
     c->last_total_recv = hb[R + E + 0];
     c->last_total_perm = hb[R + E + 1];
     c->last_total_stage = hb[R + E + 2];
+    c->totals_known = true;
     if (host_totals) {
         host_totals[0] = (int32_t)c->last_total_recv;
         host_totals[1] = (int32_t)c->last_total_perm;

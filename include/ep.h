@@ -24,8 +24,9 @@
  *     ([..][H]) and fp8 ([..][H]) must be 16-byte aligned.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  Every call is asynchronous on that stream, except
- *     ep_notify_dispatch (which waits for the receive counts, the one host
- *     synchronisation of the normal path) and the *_check calls.
+ *     ep_notify_dispatch in its waiting form (it waits for the receive
+ *     counts, the one host synchronisation of the normal path) and the
+ *     *_check calls.
  *   - bf16 values are passed as void* (2 bytes each); topk_idx is int64 with -1
  *     meaning "masked" (the entry is ignored everywhere); topk_weights fp32.
  *   - Return EP_OK or a negative ep_status; the message of the last failure on
@@ -175,13 +176,27 @@ typedef struct ep_dispatch_handle {
 
 /* Reads the layout (and topk_idx), fills the handle, and waits for the
  * receive counts ([P2] intranode_dispatch step 3, "CPU 同步等待 GPU 把接收计数写好"):
- *   host_num_recv_tokens     [R]   (required) rows each rank receives;
+ *   host_num_recv_tokens     [R]   rows each rank receives;
  *   host_num_recv_per_expert [R*L] (nullable) pairs per local expert;
  *   host_totals              [3]   (nullable) total received rows (sum over d),
  *                                  total permuted rows (P), total staged rows.
  * These host values size the caller's receive buffers.  Receive order inside
  * rank d is (source s, token t) ascending; permuted order inside rank d is
- * (local expert, s, t, k).  The node pointers are required iff N > 1. */
+ * (local expert, s, t, k).  The node pointers are required iff N > 1.
+ *
+ * No-wait form (host_num_recv_tokens, host_num_recv_per_expert and
+ * host_totals all NULL): only the two kernels are enqueued; nothing waits on
+ * the host, so the normal path (layout, notify, dispatch, permute, combine)
+ * can be captured in a CUDA graph.  This departs from the pages' host wait:
+ * the totals stay on the device (rank_base[R] received rows, perm_rank_base[R]
+ * permuted rows, stage_base[R] staged rows), and until the next waiting
+ * notify the later calls take their capacity arguments as the row bounds,
+ * size their grids from them and read the actual counts from the handle on
+ * the device.  Buffers sized for the worst case never overflow: received rows
+ * <= R*T*min(K, R), permuted rows <= R*T*K, staged rows <= R*T*min(K, N).
+ * Smaller buffers are allowed; rows past a capacity are not written and the
+ * device status reports EP_ERR_CAPACITY (ep_ctx_check).  A topk_idx value
+ * outside [-1, E) is likewise reported by ep_ctx_check. */
 ep_status ep_notify_dispatch(ep_ctx* ctx, const int64_t* topk_idx,
                              const int32_t* num_tokens_per_expert,
                              const int32_t* num_tokens_per_rank, const uint8_t* is_token_in_rank,
@@ -202,7 +217,8 @@ ep_status ep_notify_dispatch(ep_ctx* ctx, const int64_t* topk_idx,
  *   recv_topk_idx [rows][K] int32 = local expert id where expert k is on d, else -1;
  *   recv_topk_weights [rows][K] fp32 = the weight where expert k is on d, else 0.
  * recv_capacity_rows is the number of rows the recv_* arrays hold (must be
- * >= the total from the last ep_notify_dispatch, else EP_ERR_CAPACITY). */
+ * >= the total from the last waiting ep_notify_dispatch, else
+ * EP_ERR_CAPACITY; after the no-wait form the check is made on the device). */
 ep_status ep_dispatch(ep_ctx* ctx, const void* x, const int64_t* topk_idx,
                       const float* topk_weights, const ep_dispatch_handle* handle, void* recv_x,
                       int32_t* recv_src_rank, int32_t* recv_src_idx, int32_t* recv_topk_idx,
@@ -211,7 +227,9 @@ ep_status ep_dispatch(ep_ctx* ctx, const void* x, const int64_t* topk_idx,
 /* Replicates each received row once per valid local expert into contiguous
  * per-expert blocks (the grouped-GEMM layout): permuted_x [P][H] bf16 at rows
  * perm_pos, perm_src_row [P] int32 = the recv_x row each came from.
- * Reads the recv_* arrays ep_dispatch wrote (num_recv_rows of them). */
+ * Reads the recv_* arrays ep_dispatch wrote: the handle's rank_base[R] rows,
+ * read on the device; num_recv_rows (> 0) is the most it may read (the recv
+ * arrays' capacity, or the waiting notify's total). */
 ep_status ep_permute(ep_ctx* ctx, const ep_dispatch_handle* handle, const void* recv_x,
                      const int32_t* recv_src_rank, const int32_t* recv_src_idx,
                      const int32_t* recv_topk_idx, int64_t num_recv_rows, void* permuted_x,
