@@ -17,6 +17,7 @@
 // the defined order.  The partial sums are never materialised: on one GPU a
 // "partial" is the grouping of the sum.  Output: bf16, round to nearest even.
 #include <climits>
+#include <cstdlib>
 
 #include "ep_internal.cuh"
 #include "ep_combine.cuh"
@@ -47,7 +48,7 @@ __device__ __forceinline__ int4 f32x8_to_bf16(const float* f) {
 
 // MODE 0: flat (rank partials), 1: hierarchical (rank, node, final), 2: low-latency (k order)
 template <int KMAX, int MODE>
-__global__ void __launch_bounds__(kCombineThreads, KMAX <= 8 ? 3 : 1) combine_kernel(CombineArgs a) {
+__global__ void __launch_bounds__(kCombineThreads, KMAX <= 8 ? (MODE == 2 ? 2 : 3) : 1) combine_kernel(CombineArgs a) {
     __shared__ int64_t sh_row[kCombineWarps][KMAX];
     __shared__ float sh_w[kCombineWarps][KMAX];
     __shared__ uint8_t sh_brk[kCombineWarps][KMAX];  // bit0: new rank group, bit1: new node group
@@ -60,7 +61,24 @@ __global__ void __launch_bounds__(kCombineThreads, KMAX <= 8 ? 3 : 1) combine_ke
     // per token so that enough loads are in flight
     const int per = (nvec + a.splits - 1) / a.splits;
     const int64_t n_items = n_tok * a.splits;
-    for (int64_t q = (int64_t)blockIdx.x * kCombineWarps + warp; q < n_items; q += (int64_t)gridDim.x * kCombineWarps) {
+    const int64_t stride = (int64_t)gridDim.x * kCombineWarps;
+    // The entry loads of a warp's next item are issued before the current
+    // item's row loads, so that they arrive while the rows stream in (otherwise
+    // every item would start with idle dependent loads).
+    auto token_of = [&](int64_t q) -> int64_t {
+        const int64_t tok = q / a.splits;
+        return (int64_t)(tok / a.n) * a.T + a.t0 + (int)(tok % a.n);
+    };
+    int64_t nx_e = -1, nx_aux = -1;  // topk_idx and perm_pos / slot of the next item's entry `lane`
+    float nx_w = 0.0f;
+    int64_t q = (int64_t)blockIdx.x * kCombineWarps + warp;
+    if (q < n_items && lane < K) {
+        const int64_t g = token_of(q);
+        nx_e = a.topk_idx[g * K + lane];
+        nx_w = a.w[g * K + lane];
+        nx_aux = MODE == 2 ? a.slot[g * K + lane] : a.perm_pos[g * K + lane];
+    }
+    for (; q < n_items; q += stride) {
         const int64_t tok = q / a.splits;
         const int c_lo = (int)(q % a.splits) * per;
         const int c_hi = min(nvec, c_lo + per);
@@ -73,22 +91,28 @@ __global__ void __launch_bounds__(kCombineThreads, KMAX <= 8 ? 3 : 1) combine_ke
         int64_t row = 0;
         float wk = 0.0f;
         if (lane < K) {
-            const int64_t e = a.topk_idx[g * K + lane];
+            const int64_t e = nx_e;
             if (e >= 0 && e < a.E) {
                 d = (int)(e / a.L);
                 if (MODE == 2) {
                     const int l = (int)(e % a.L);
-                    const int32_t sl = a.slot[g * K + lane];
+                    const int32_t sl = (int32_t)nx_aux;
                     const int32_t begin = a.layout_range[(((int64_t)d * a.L + l) * a.R + s) * 2];
                     row = ((int64_t)d * a.L + l) * a.rows_per_expert + begin + sl;
                     valid = sl >= 0 && row >= 0 && row < a.y_rows;
                 } else {
-                    row = a.perm_pos[g * K + lane];
+                    row = nx_aux;
                     valid = row >= 0 && row < a.y_rows;
                 }
                 if (!valid) flag(a.status, FLAG_BOUNDS);
-                wk = a.w[g * K + lane];
+                wk = nx_w;
             }
+        }
+        if (q + stride < n_items && lane < K) {  // the next item's entries, in flight from here on
+            const int64_t gn = token_of(q + stride);
+            nx_e = a.topk_idx[gn * K + lane];
+            nx_w = a.w[gn * K + lane];
+            nx_aux = MODE == 2 ? a.slot[gn * K + lane] : a.perm_pos[gn * K + lane];
         }
         const int key = valid ? (MODE == 2 ? lane : d * 32 + lane) : INT_MAX;
         int rank = 0;
@@ -122,6 +146,41 @@ __global__ void __launch_bounds__(kCombineThreads, KMAX <= 8 ? 3 : 1) combine_ke
         const uint8_t* y = static_cast<const uint8_t*>(a.y);
         int4* out = reinterpret_cast<int4*>(static_cast<uint8_t*>(a.out) + g * row_bytes);
         // ---- channels ------------------------------------------------------------------
+        if (MODE == 2) {
+            // k order, one fp32 chain per channel: two vectors per lane per step,
+            // every load of the step issued before the first is used
+            for (int c = c_lo + lane; c < c_hi; c += 64) {
+                const bool two = c + 32 < c_hi;
+                int4 v0[KMAX], v1[KMAX];
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    if (j < nvalid) {
+                        v0[j] = ld_nc_na_v4(y + roff[j] + (int64_t)c * 16);
+                        if (two) v1[j] = ld_nc_na_v4(y + roff[j] + (int64_t)(c + 32) * 16);
+                    }
+                }
+                float p0[8], p1[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) p0[i] = p1[i] = 0.0f;
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    if (j < nvalid) {
+                        float yv[8];
+                        bf16x8_to_f32(v0[j], yv);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) p0[i] = __fmaf_rn(wr[j], yv[i], p0[i]);
+                        if (two) {
+                            bf16x8_to_f32(v1[j], yv);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) p1[i] = __fmaf_rn(wr[j], yv[i], p1[i]);
+                        }
+                    }
+                }
+                st_na_v4(out + c, f32x8_to_bf16(p0));
+                if (two) st_na_v4(out + c + 32, f32x8_to_bf16(p1));
+            }
+            continue;
+        }
         for (int c = c_lo + lane; c < c_hi; c += 32) {
             int4 v[KMAX];
 #pragma unroll
@@ -184,25 +243,26 @@ ep_status launch_combine(const CombineArgs& a, int mode, int num_sms, cudaStream
     const int64_t n_tok = (int64_t)a.R * a.n;
     if (n_tok <= 0) return EP_OK;
     CombineArgs b = a;
-    // Work items are (token, channel slice).  The grid holds `conc` resident
-    // warps; pick the number of slices per token (1..8, at least one 16-byte
-    // vector per lane per slice) whose items fill the last round of warps best,
-    // preferring fewer slices (each slice reloads the token's entries).
+    // Work items are (token, channel slice).  A slice reloads the token's
+    // entries, so use the fewest slices per token that still give about three
+    // quarters of the resident warps an item (measured on the decode batch:
+    // 1-2 slices 49 us, 7 slices 53 us, 8 slices 57 us).
     const int nvec = a.H / 8;
-    const int64_t conc = (int64_t)num_sms * 3 * kCombineWarps;
+    const int64_t conc = (int64_t)num_sms * (mode == 2 ? 2 : 3) * kCombineWarps;  // resident warps
     int max_splits = nvec / 32 < 8 ? nvec / 32 : 8;
     if (max_splits < 1) max_splits = 1;
-    int splits = 1;
-    double best = -1.0;
+    int splits = max_splits;
     for (int sp = 1; sp <= max_splits; ++sp) {
-        const int64_t items = n_tok * sp;
-        const int64_t rounds = (items + conc - 1) / conc;
-        const double eff = (double)items / (double)(rounds * conc);
-        if (eff > best + 0.03) {
-            best = eff;
+        if (n_tok * sp * 4 >= conc * 3) {
             splits = sp;
+            break;
         }
     }
+    static const int forced = [] {  // EP_COMBINE_SPLITS: launch-shape override for sweeps
+        const char* v = getenv("EP_COMBINE_SPLITS");
+        return v ? atoi(v) : 0;
+    }();
+    if (forced >= 1 && forced <= max_splits) splits = forced;
     b.splits = splits;
     const int64_t items = n_tok * splits;
     int64_t want = (items + kCombineWarps - 1) / kCombineWarps;

@@ -68,3 +68,56 @@ def test_fp8_needs_hidden_multiple_of_128():
     from combine_get_dispatch_histograms_gb300 import EpError
     with pytest.raises(EpError):
         ctx.quantize_fp8(torch.zeros(2, 4, 136, dtype=torch.bfloat16, device="cuda"))
+
+
+def _bf16_values_up_to(a_bits: int) -> np.ndarray:
+    """Every finite bf16 value v with |v| <= the bf16 value a, both signs (bit patterns)."""
+    pos = np.arange(0, 0x7f80, dtype=np.uint32)
+    mag = (pos << 16).view(np.float32)
+    a = np.array([a_bits << 16], np.uint32).view(np.float32)[0]
+    keep = pos[mag <= a].astype(np.uint16)
+    return np.concatenate([keep, keep | np.uint16(0x8000)])
+
+
+def test_quantize_every_bf16_value_for_many_scales():
+    """Exhaustive over x: for each block maximum a (so scale = a / 448), every
+    bf16 value with |x| <= a, in blocks of 128 led by a; codes and scales
+    bit-exact against the oracle, on the normal-mode quantiser and on the
+    low-latency send (both use the same codec)."""
+    rng = np.random.default_rng(5)
+    special = [0x43e0, 0x4360, 0x4460,  # 448, 224, 896: scales 1, 1/2, 2 (exact quotients, e4m3 ties)
+               0x3f80, 0x4040, 0x4030, 0x3e99, 0x3a83, 0x3c8c, 0x40a0, 0x40e0, 0x449a,
+               0x7f7f,  # largest finite bf16
+               0x0080,  # smallest normal bf16
+               0x0001, 0x0040]  # subnormal block maxima
+    amaxes = special + [int(b) for b in rng.integers(0x2000, 0x5000, size=10)]
+    blocks = []
+    for a in amaxes:
+        vals = _bf16_values_up_to(a)
+        vals = vals[np.argsort(rng.random(len(vals)))]
+        nb = -(-len(vals) // 127)
+        pad = np.zeros(nb * 127, np.uint16)
+        pad[:len(vals)] = vals
+        blk = np.concatenate([np.full((nb, 1), a, np.uint16), pad.reshape(nb, 127)], axis=1)
+        blocks.append(blk)
+    blocks = np.concatenate(blocks)
+    H = 128 * 64
+    T = -(-blocks.shape[0] // 64)
+    allb = np.zeros((T * 64, 128), np.uint16)
+    allb[:blocks.shape[0]] = blocks
+    xb = allb.reshape(T, H)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).reshape(1, T, H)
+    o_rows = np.stack([np.concatenate([c, s.view(np.uint8)]) for c, s in map(orc.quantize_row, xb)])
+    n_def = H + H // 32
+    # normal-mode quantiser
+    ctx = Context(1, 1, 1, T, H, num_channels=1)
+    xq = ctx.quantize_fp8(x.cuda())
+    ctx.check()
+    eq(bits(xq)[:, :n_def], o_rows, "fp8 rows (exhaustive bf16 x)")
+    # low-latency send: one rank, one expert, every token sent once (slot = t)
+    from combine_get_dispatch_histograms_gb300 import LLBuffer
+    buf = LLBuffer(1, 1, 1, T, H, T)
+    pk = buf.dispatch(x.cuda(), torch.zeros(1, T, 1, dtype=torch.int64, device="cuda"))
+    buf.check()
+    eq(pk["packed_x"][0, 0, :T], o_rows[:, :H], "LL message codes (exhaustive bf16 x)")
+    eq(pk["packed_scales"][0, 0, :T], o_rows[:, H:].view(np.float32), "LL message scales")
