@@ -215,6 +215,8 @@ def run_ll_only(args):
     dw = inputs.WORKLOADS["decode"]
     if args.ll_tokens:
         dw = dw.replace(T=args.ll_tokens, ll_cap=args.ll_tokens)
+    if args.ll_experts:
+        dw = dw.replace(E=args.ll_experts)
     idx, wt = inputs.make_routing(dw, 7)
     x = inputs.make_x(dw, 7, device="cuda")
     idxd, wd = idx.cuda(), wt.cuda()
@@ -285,6 +287,8 @@ def main():
     ap.add_argument("--ll-only", action="store_true",
                     help="profiling mode: only the low-latency decode layer (no contract line)")
     ap.add_argument("--ll-tokens", type=int, default=0, help="with --ll-only: T = cap of the decode layer")
+    ap.add_argument("--ll-experts", type=int, default=0,
+                    help="with --ll-only: E of the decode layer (fewer experts: same messages, smaller buffers)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
