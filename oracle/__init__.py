@@ -71,6 +71,8 @@ def _declare(L):
         "orc_notify": (I, [I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P]),
         "orc_dispatch": (I, [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P]),
         "orc_permute": (I, [I, I, I, I, I, P, P, P, P, P, P, P]),
+        "orc_notify_aligned": (I, [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P]),
+        "orc_permute_aligned": (I, [I, I, I, I, I, I, ctypes.c_int64, P, P, P, P, P, P, P]),
         "orc_combine_ord32": (I, [I, I, I, I, I, P, P, P, P, P]),
         "orc_combine_ref64": (I, [I, I, I, I, I, P, P, P, P, P]),
         "orc_ll_send": (I, [I, I, I, I, I, I, I, I, P, P, P, P, P, P, P]),
@@ -193,7 +195,7 @@ def layout(topk_idx, R: int, E: int, num_nodes: int = 0):
     return out
 
 
-def notify(lay: dict, R: int, E: int, T: int, C: int):
+def notify(lay: dict, R: int, E: int, T: int, C: int, align: int = 1):
     L = E // R
     o = dict(
         recv_count=np.empty((R, R), np.int32),
@@ -209,11 +211,18 @@ def notify(lay: dict, R: int, E: int, T: int, C: int):
     ntpe = _np(lay["num_tokens_per_expert"], np.int32)
     ntpr = _np(lay["num_tokens_per_rank"], np.int32)
     itir = _np(lay["is_token_in_rank"], np.uint8)
-    rc = lib().orc_notify(R, E, T, C, _p(ntpe), _p(ntpr), _p(itir), _p(o["recv_count"]),
-                          _p(o["num_recv_tokens"]), _p(o["recv_offsets"]), _p(o["rank_base"]),
-                          _p(o["num_recv_per_expert"]), _p(o["expert_offsets"]),
-                          _p(o["perm_rank_base"]), _p(o["channel_prefix_matrix"]), _p(o["send_pos"]))
+    if align == 1:
+        rc = lib().orc_notify(R, E, T, C, _p(ntpe), _p(ntpr), _p(itir), _p(o["recv_count"]),
+                              _p(o["num_recv_tokens"]), _p(o["recv_offsets"]), _p(o["rank_base"]),
+                              _p(o["num_recv_per_expert"]), _p(o["expert_offsets"]),
+                              _p(o["perm_rank_base"]), _p(o["channel_prefix_matrix"]), _p(o["send_pos"]))
+    else:
+        rc = lib().orc_notify_aligned(R, E, T, C, align, _p(ntpe), _p(ntpr), _p(itir), _p(o["recv_count"]),
+                                      _p(o["num_recv_tokens"]), _p(o["recv_offsets"]), _p(o["rank_base"]),
+                                      _p(o["num_recv_per_expert"]), _p(o["expert_offsets"]),
+                                      _p(o["perm_rank_base"]), _p(o["channel_prefix_matrix"]), _p(o["send_pos"]))
     _ok("orc_notify", rc)
+    o["align"] = align
     return o
 
 
@@ -249,9 +258,15 @@ def permute(topk_idx, recv_x, note: dict, R: int, E: int):
         perm_src_row=np.empty(P, np.int32),
         perm_pos=np.empty((R, T, K), np.int32),
     )
-    rc = lib().orc_permute(R, E, K, T, H, _p(idx), _p(rx), _p(_np(note["rank_base"], np.int32)),
-                           _p(_np(note["send_pos"], np.int32)), _p(o["permuted_x"]), _p(o["perm_src_row"]),
-                           _p(o["perm_pos"]))
+    align = int(note.get("align", 1))
+    if align == 1:
+        rc = lib().orc_permute(R, E, K, T, H, _p(idx), _p(rx), _p(_np(note["rank_base"], np.int32)),
+                               _p(_np(note["send_pos"], np.int32)), _p(o["permuted_x"]), _p(o["perm_src_row"]),
+                               _p(o["perm_pos"]))
+    else:
+        rc = lib().orc_permute_aligned(R, E, K, T, H, align, P, _p(idx), _p(rx),
+                                       _p(_np(note["rank_base"], np.int32)), _p(_np(note["send_pos"], np.int32)),
+                                       _p(o["permuted_x"]), _p(o["perm_src_row"]), _p(o["perm_pos"]))
     _ok("orc_permute", rc)
     return o
 

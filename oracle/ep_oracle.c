@@ -186,7 +186,19 @@ int orc_notify(int R, int E, int T, int C, const int32_t* ntpe, const int32_t* n
                int32_t* recv_offsets, int32_t* rank_base, int32_t* num_recv_per_expert,
                int32_t* expert_offsets, int32_t* perm_rank_base, int32_t* cpm,
                int32_t* send_pos) {
-    if (R <= 0 || E <= 0 || E % R != 0 || T < 0 || C <= 0) return -1;
+    return orc_notify_aligned(R, E, T, C, 1, ntpe, ntpr, itir, recv_count, num_recv_tokens, recv_offsets,
+                              rank_base, num_recv_per_expert, expert_offsets, perm_rank_base, cpm, send_pos);
+}
+
+/* round n up to a multiple of a (a >= 1) */
+static int32_t round_up(int32_t n, int a) { return (n + a - 1) / a * a; }
+
+int orc_notify_aligned(int R, int E, int T, int C, int align, const int32_t* ntpe, const int32_t* ntpr,
+                       const uint8_t* itir, int32_t* recv_count, int32_t* num_recv_tokens,
+                       int32_t* recv_offsets, int32_t* rank_base, int32_t* num_recv_per_expert,
+                       int32_t* expert_offsets, int32_t* perm_rank_base, int32_t* cpm,
+                       int32_t* send_pos) {
+    if (R <= 0 || E <= 0 || E % R != 0 || T < 0 || C <= 0 || align < 1) return -1;
     const int L = E / R;
     /* all-gather of the per-peer counts, seen from each receiver d */
     for (int d = 0; d < R; ++d)
@@ -202,7 +214,9 @@ int orc_notify(int R, int E, int T, int C, const int32_t* ntpe, const int32_t* n
     }
     rank_base[0] = 0;
     for (int d = 0; d < R; ++d) rank_base[d + 1] = rank_base[d] + num_recv_tokens[d];
-    /* per local expert totals and offsets */
+    /* per local expert totals and offsets; with an expert alignment a > 1
+     * every expert's block takes its count rounded up to a multiple of a rows
+     * (the tail rows are padding), so every block starts at a multiple of a */
     perm_rank_base[0] = 0;
     for (int d = 0; d < R; ++d) {
         int32_t acc = 0;
@@ -211,7 +225,7 @@ int orc_notify(int R, int E, int T, int C, const int32_t* ntpe, const int32_t* n
             for (int s = 0; s < R; ++s) n += ntpe[s * E + d * L + l];
             num_recv_per_expert[d * L + l] = n;
             expert_offsets[d * L + l] = acc;
-            acc += n;
+            acc += round_up(n, align);
         }
         perm_rank_base[d + 1] = perm_rank_base[d] + acc;
     }
@@ -295,7 +309,19 @@ static int pair_cmp(const void* a, const void* b) {
 int orc_permute(int R, int E, int K, int T, int H, const int64_t* topk_idx, const uint16_t* recv_x,
                 const int32_t* rank_base, const int32_t* send_pos, uint16_t* permuted_x,
                 int32_t* perm_src_row, int32_t* perm_pos) {
-    if (check_shape(R, E, K, T) || H <= 0) return -1;
+    return orc_permute_aligned(R, E, K, T, H, 1, -1, topk_idx, recv_x, rank_base, send_pos, permuted_x,
+                               perm_src_row, perm_pos);
+}
+
+/* As orc_permute, each (d, l) block taking its pair count rounded up to a
+ * multiple of align rows: pairs keep their (d, l, s, t, k) order, the block
+ * of (d, l) starts at the sum of the rounded counts of the blocks before it,
+ * and padding rows get perm_src_row = -1 (permuted_x rows left as they are).
+ * rows = the number of rows the outputs hold (checked), or -1 to skip. */
+int orc_permute_aligned(int R, int E, int K, int T, int H, int align, int64_t rows, const int64_t* topk_idx,
+                        const uint16_t* recv_x, const int32_t* rank_base, const int32_t* send_pos,
+                        uint16_t* permuted_x, int32_t* perm_src_row, int32_t* perm_pos) {
+    if (check_shape(R, E, K, T) || H <= 0 || align < 1) return -1;
     const int L = E / R;
     int64_t P = 0;
     for (int64_t i = 0; i < (int64_t)R * T * K; ++i)
@@ -314,15 +340,31 @@ int orc_permute(int R, int E, int K, int T, int H, const int64_t* topk_idx, cons
                 pairs[n++] = p;
             }
     qsort(pairs, (size_t)n, sizeof(pair_t), pair_cmp);
-    for (int64_t i = 0; i < n; ++i) {
-        const pair_t* p = &pairs[i];
-        int32_t sp = send_pos[((int64_t)p->s * T + p->t) * R + p->d];
-        int64_t src = (int64_t)rank_base[p->d] + sp;
-        memcpy(permuted_x + i * H, recv_x + src * H, sizeof(uint16_t) * (size_t)H);
-        perm_src_row[i] = (int32_t)src;
-        perm_pos[((int64_t)p->s * T + p->t) * K + p->k] = (int32_t)i;
+    /* walk the sorted pairs block by block: a block is a run of equal (d, l);
+     * empty blocks take no rows, so only the runs present advance the row */
+    int64_t row = 0;
+    for (int64_t i = 0; i < n;) {
+        int64_t j = i;
+        while (j < n && pairs[j].d == pairs[i].d && pairs[j].l == pairs[i].l) ++j;
+        const int64_t cnt = j - i, padded = (cnt + align - 1) / align * align;
+        if (rows >= 0 && row + padded > rows) {
+            free(pairs);
+            return -1;
+        }
+        for (int64_t q = 0; q < cnt; ++q) {
+            const pair_t* p = &pairs[i + q];
+            int32_t sp = send_pos[((int64_t)p->s * T + p->t) * R + p->d];
+            int64_t src = (int64_t)rank_base[p->d] + sp;
+            memcpy(permuted_x + (row + q) * H, recv_x + src * H, sizeof(uint16_t) * (size_t)H);
+            perm_src_row[row + q] = (int32_t)src;
+            perm_pos[((int64_t)p->s * T + p->t) * K + p->k] = (int32_t)(row + q);
+        }
+        for (int64_t q = cnt; q < padded; ++q) perm_src_row[row + q] = -1;
+        row += padded;
+        i = j;
     }
     free(pairs);
+    if (rows >= 0 && row != rows) return -1;
     return 0;
 }
 

@@ -48,6 +48,15 @@ int orc_notify(int R, int E, int T, int C,
                int32_t* perm_rank_base /*[R+1]*/, int32_t* channel_prefix_matrix /*[R][R][C]*/,
                int32_t* send_pos /*[R][T][R]*/);
 
+/* As orc_notify; every (d, l) block of the permuted layout takes its count
+ * rounded up to a multiple of align rows (expert_offsets, perm_rank_base). */
+int orc_notify_aligned(int R, int E, int T, int C, int align,
+                       const int32_t* num_tokens_per_expert, const int32_t* num_tokens_per_rank,
+                       const uint8_t* is_token_in_rank, int32_t* recv_count, int32_t* num_recv_tokens,
+                       int32_t* recv_offsets, int32_t* rank_base, int32_t* num_recv_per_expert,
+                       int32_t* expert_offsets, int32_t* perm_rank_base, int32_t* channel_prefix_matrix,
+                       int32_t* send_pos);
+
 /* ---- dispatch scatter (one copy per destination rank) ------------------- */
 int orc_dispatch(int R, int E, int K, int T, int H,
                  const uint16_t* x, const int64_t* topk_idx, const float* topk_weights,
@@ -60,6 +69,10 @@ int orc_permute(int R, int E, int K, int T, int H, const int64_t* topk_idx,
                 const uint16_t* recv_x, const int32_t* rank_base, const int32_t* send_pos,
                 uint16_t* permuted_x /*[P][H]*/, int32_t* perm_src_row /*[P]*/,
                 int32_t* perm_pos /*[R][T][K]*/);
+/* Aligned blocks: padding rows get perm_src_row -1; rows = output rows or -1. */
+int orc_permute_aligned(int R, int E, int K, int T, int H, int align, int64_t rows, const int64_t* topk_idx,
+                        const uint16_t* recv_x, const int32_t* rank_base, const int32_t* send_pos,
+                        uint16_t* permuted_x, int32_t* perm_src_row, int32_t* perm_pos);
 
 /* ---- combine ------------------------------------------------------------ */
 /* fp32 fmaf in the defined order: per destination rank d ascending, the rank

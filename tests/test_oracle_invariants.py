@@ -185,3 +185,56 @@ def test_invalid_topk_reported(orc):
     with pytest.raises(orc.OracleError) as e:
         orc.layout(idx, 2, 4)
     assert e.value.code == -2
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"c{c[-1]}" for c in CASES])
+@pytest.mark.parametrize("align", [1, 3, 16, 128])
+def test_expert_alignment(orc, case, align):
+    """Expert-aligned permuted layout: every (rank, local expert) block starts at
+    a multiple of the alignment inside its rank and takes its count rounded up;
+    dropping the padding rows gives the unaligned layout row for row; padding
+    rows are marked -1 and referenced by no pair; everything else in the
+    handle is as without alignment."""
+    R, E, K, T, H, C, mask_p, distinct, seed = case
+    idx, x, w, lay, note1, disp, perm1 = _run(orc, *case)
+    L = E // R
+    note = orc.notify(lay, R, E, T, C, align=align)
+    for k in ("recv_count", "num_recv_tokens", "recv_offsets", "rank_base", "num_recv_per_expert",
+              "channel_prefix_matrix", "send_pos"):
+        assert np.array_equal(note[k], note1[k]), k
+    cnt = note["num_recv_per_expert"].astype(np.int64)
+    padded = (cnt + align - 1) // align * align
+    eo = note["expert_offsets"].astype(np.int64)
+    assert (eo % align == 0).all()
+    assert (eo[:, 0] == 0).all()
+    assert np.array_equal(eo[:, 1:] - eo[:, :-1], padded[:, :-1])
+    prb = note["perm_rank_base"].astype(np.int64)
+    assert prb[0] == 0 and np.array_equal(np.diff(prb), padded.sum(axis=1))
+    if align == 1:
+        assert np.array_equal(eo, note1["expert_offsets"]) and np.array_equal(prb, note1["perm_rank_base"])
+    perm = orc.permute(idx, disp["recv_x"], note, R, E)
+    pp = perm["perm_pos"]
+    psr = perm["perm_src_row"]
+    P = int(prb[R])
+    assert psr.shape == (P,)
+    # every pair lands inside its own block, in (s, t, k) order
+    used = np.zeros(P, bool)
+    last = {}
+    for s, t, k in zip(*np.nonzero(idx >= 0)):
+        e = int(idx[s, t, k])
+        d, l = divmod(e, L)
+        r = int(pp[s, t, k])
+        lo = prb[d] + eo[d, l]
+        assert lo <= r < lo + cnt[d, l], (s, t, k)
+        assert not used[r]
+        used[r] = True
+        assert last.get((d, l), -1) < r
+        last[(d, l)] = r
+    assert np.array_equal(psr >= 0, used)
+    # without the padding rows: the unaligned layout, row for row
+    assert np.array_equal(psr[used], perm1["perm_src_row"])
+    assert np.array_equal(perm["permuted_x"][used], perm1["permuted_x"])
+    # the unaligned perm_pos is the aligned one renumbered over the used rows
+    rank_of = np.cumsum(used) - 1
+    valid = idx >= 0
+    assert np.array_equal(rank_of[pp[valid]], perm1["perm_pos"][valid])
