@@ -87,7 +87,7 @@ class Context:
     """Normal (high-throughput) mode over R virtual ranks on one GPU."""
 
     def __init__(self, num_ranks: int, num_experts: int, num_topk: int, num_tokens: int, hidden: int,
-                 num_channels: int = 8, num_nodes: int = 1, device=None):
+                 num_channels: int = 8, num_nodes: int = 1, device=None, expert_alignment: int = 1):
         if not torch.cuda.is_available():
             raise RuntimeError("the EP library needs a CUDA GPU")
         self.lib = _lib.load()
@@ -99,6 +99,9 @@ class Context:
         self._ctx = ctypes.c_void_p()
         with torch.cuda.device(self.device):
             check("ep_ctx_create", self.lib.ep_ctx_create(ctypes.byref(self.cfg), ctypes.byref(self._ctx)))
+        self.expert_alignment = 1
+        if expert_alignment != 1:
+            self.set_expert_alignment(expert_alignment)
         self._host_recv = (ctypes.c_int32 * num_ranks)()
         self._host_exp = (ctypes.c_int32 * num_experts)()
         self._host_tot = (ctypes.c_int32 * 3)()
@@ -126,6 +129,12 @@ class Context:
 
     def check(self, stream=None):
         check("ep_ctx_check", self.lib.ep_ctx_check(self._ctx, _stream(stream)))
+
+    def set_expert_alignment(self, alignment: int):
+        """Round every permuted expert block up to a multiple of `alignment` rows
+        (from the next notify on); padding rows are left unwritten."""
+        check("ep_ctx_set_expert_alignment", self.lib.ep_ctx_set_expert_alignment(self._ctx, int(alignment)))
+        self.expert_alignment = int(alignment)
 
     # ---- layout ----------------------------------------------------------------
     def get_dispatch_layout(self, topk_idx: torch.Tensor, nodes: Optional[bool] = None, stream=None, out=None):
@@ -165,7 +174,8 @@ class Context:
         """Worst-case (received, permuted, staged) row counts: buffers of these
         sizes never overflow, whatever the routing."""
         R, T, K, N = self.R, self.T, self.K, self.N
-        return R * T * min(K, R), R * T * K, (R * T * min(K, N) if N > 1 else 0)
+        pad = self.E * (self.expert_alignment - 1)
+        return R * T * min(K, R), R * T * K + pad, (R * T * min(K, N) if N > 1 else 0)
 
     def notify_dispatch(self, topk_idx: torch.Tensor, layout: dict, stream=None, handle: Optional[Handle] = None,
                         wait: bool = True) -> Handle:

@@ -102,6 +102,7 @@ struct ep_ctx {
     // totals of the last notify (host copies), sizes of later launches
     int64_t last_total_recv, last_total_perm, last_total_stage;
     bool totals_known;  // false after a notify that did not wait for the counts
+    int expert_alignment;  // rows of each permuted expert block are rounded up to this
     int last_launches;
 };
 

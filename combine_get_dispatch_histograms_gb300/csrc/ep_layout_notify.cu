@@ -159,6 +159,7 @@ struct NotifyArgs {
     const uint8_t* itin;
     ep_dispatch_handle h;
     int R, E, K, T, L, N, G;
+    int align;       // expert alignment of the permuted blocks (1 = none)
     TileGeom geom;
     int32_t* part;   // [R][tiles][E + R + N]
     int32_t* ebase;  // [R][E]
@@ -235,21 +236,25 @@ __device__ void notify_global_scan(const NotifyArgs& a, int32_t* sh /* >= 2E + 3
         rbase[R] = acc;
         sh_total_recv = acc;
     }
-    // (c) exclusive scan over experts in (d, l) order: contiguous chunk per thread
+    // (c) exclusive scan over experts in (d, l) order: contiguous chunk per
+    // thread; each expert's block takes its count rounded up to the alignment
     const int per = (E + blockDim.x - 1) / blockDim.x;
     const int e0 = threadIdx.x * per;
+    const int al = a.align;
+    auto rows_of = [al](int32_t n) -> int32_t { return (n + al - 1) / al * al; };
     int32_t local = 0;
-    for (int e = e0; e < e0 + per && e < E; ++e) local += tot[e];
+    for (int e = e0; e < e0 + per && e < E; ++e) local += rows_of(tot[e]);
     int32_t run = block_exclusive_scan(local, scan_tmp);
     for (int e = e0; e < e0 + per && e < E; ++e) {
         off[e] = run;
-        run += tot[e];
+        run += rows_of(tot[e]);
     }
     __syncthreads();
-    if (threadIdx.x == 0) sh_total_perm = off[E - 1] + tot[E - 1];
+    const int32_t total_perm = off[E - 1] + rows_of(tot[E - 1]);
+    if (threadIdx.x == 0) sh_total_perm = total_perm;
     for (int d = threadIdx.x; d <= R; d += blockDim.x) {
         a.h.rank_base[d] = rbase[d];
-        a.h.perm_rank_base[d] = d < R ? off[d * L] : off[E - 1] + tot[E - 1];
+        a.h.perm_rank_base[d] = d < R ? off[d * L] : total_perm;
     }
     // (d) per expert: offsets inside the rank, and the first permuted row of
     // every (source, expert) = the expert's first row + earlier sources' pairs
@@ -547,6 +552,7 @@ extern "C" ep_status ep_ctx_create(const ep_config* cfg, ep_ctx** out) {
     if (st != EP_OK) return st;
     ep_ctx* c = new ep_ctx();
     c->totals_known = true;  // nothing notified yet: zero rows
+    c->expert_alignment = 1;
     std::memset(c, 0, sizeof(*c));
     c->cfg = *cfg;
     c->L = cfg->num_experts / cfg->num_ranks;
@@ -625,6 +631,12 @@ extern "C" ep_status ep_ctx_check(ep_ctx* c, void* stream) {
 extern "C" ep_status ep_ctx_set_wait_timeout_us(ep_ctx* c, int64_t us) {
     if (!c || us <= 0) return set_error(EP_ERR_INVALID_ARG, "bad context or timeout");
     c->wait_timeout_ns = us * 1000;
+    return EP_OK;
+}
+
+extern "C" ep_status ep_ctx_set_expert_alignment(ep_ctx* c, int32_t alignment) {
+    if (!c || alignment < 1 || alignment > (1 << 16)) return set_error(EP_ERR_INVALID_ARG, "bad context or alignment");
+    c->expert_alignment = alignment;
     return EP_OK;
 }
 
@@ -753,6 +765,7 @@ extern "C" ep_status ep_notify_dispatch(ep_ctx* c, const int64_t* topk_idx, cons
     a.L = c->L;
     a.N = hier ? f.num_nodes : 0;
     a.G = c->G;
+    a.align = c->expert_alignment;
     a.geom = c->tiles;
     a.part = c->ws_notify_part;
     a.ebase = c->ws_ebase;

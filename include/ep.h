@@ -93,6 +93,18 @@ ep_status ep_ctx_check(ep_ctx* ctx, void* stream);
  * (copy-pipeline barriers).  Default 2 000 000. */
 ep_status ep_ctx_set_wait_timeout_us(ep_ctx* ctx, int64_t us);
 
+/* Expert alignment of the permuted layout (default 1 = none; 1..65536).
+ * The pages fix none; it serves a grouped GEMM that wants every expert's
+ * block to start on a tile boundary.  From the next ep_notify_dispatch on,
+ * each (rank d, local expert l) block of the permuted layout takes
+ * num_recv_per_expert[d][l] rounded up to a multiple of `alignment` rows:
+ * expert_offsets[d][l] (a multiple of the alignment), perm_rank_base and
+ * the permuted totals include the padding; num_recv_per_expert stays the
+ * pair count.  The pairs fill the first rows of their block in the usual
+ * order; padding rows of permuted_x, perm_src_row, perm_src_token and
+ * perm_weight are not written.  Combine reads only the pairs' rows. */
+ep_status ep_ctx_set_expert_alignment(ep_ctx* ctx, int32_t alignment);
+
 /* Number of kernel launches the last call on this context made (for the
  * bench's launch count). */
 int32_t ep_ctx_last_launches(const ep_ctx* ctx);
@@ -193,7 +205,8 @@ typedef struct ep_dispatch_handle {
  * notify the later calls take their capacity arguments as the row bounds,
  * size their grids from them and read the actual counts from the handle on
  * the device.  Buffers sized for the worst case never overflow: received rows
- * <= R*T*min(K, R), permuted rows <= R*T*K, staged rows <= R*T*min(K, N).
+ * <= R*T*min(K, R), permuted rows <= R*T*K (plus E*(alignment-1) with an
+ * expert alignment), staged rows <= R*T*min(K, N).
  * Smaller buffers are allowed; rows past a capacity are not written and the
  * device status reports EP_ERR_CAPACITY (ep_ctx_check).  A topk_idx value
  * outside [-1, E) is likewise reported by ep_ctx_check. */

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle as orc
-from combine_get_dispatch_histograms_gb300 import inputs
+from combine_get_dispatch_histograms_gb300 import LLBuffer, inputs
 from parity_util import compare_normal, eq, run_gpu_ll, bits
 
 pytestmark = pytest.mark.gpu
@@ -181,3 +181,49 @@ def test_low_latency_layer_in_cuda_graph():
         buf.check()
         eq(out, o_out, "graph replay")
         eq(pk["packed_recv_count"], o_pk["packed_recv_count"], "graph replay counts")
+
+
+def test_two_microbatches_on_two_streams():
+    """Dual-microbatch overlap: two low-latency buffers, each sending, receiving
+    and combining its own microbatch on its own stream at the same time, give
+    the results each gives alone (nothing waits across the streams)."""
+    R, E, K, T, H, cap = 8, 64, 8, 96, 256, 96
+    bufs = [LLBuffer(R, E, K, T, H, cap) for _ in range(2)]
+    ins = []
+    for seed in (31, 32):
+        idx = inputs.random_topk(R, E, K, T, seed, 0.05)
+        ins.append((inputs.random_x(R, T, H, seed).cuda(), idx.cuda(),
+                    inputs.random_weights(R, T, K, seed).cuda()))
+    # alone, one after the other
+    alone = []
+    for b, (x, idx, w) in zip(bufs, ins):
+        pk = b.dispatch(x, idx)
+        y = torch.randn(pk["packed_x"].shape, generator=torch.Generator(device="cuda").manual_seed(5),
+                        device="cuda").to(torch.bfloat16)
+        out = b.combine(y, idx, w, pk)
+        torch.cuda.synchronize()
+        b.check()
+        alone.append(({k: v.clone() for k, v in pk.items()}, y, out.clone()))
+    # together, on two streams
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    main = torch.cuda.current_stream()
+    res = []
+    for st, b, (x, idx, w), (_, y, _) in zip(streams, bufs, ins, alone):
+        st.wait_stream(main)
+        with torch.cuda.stream(st):
+            pk = b.dispatch(x, idx)
+            out = b.combine(y, idx, w, pk)
+        res.append((pk, out))
+    for st in streams:
+        main.wait_stream(st)
+    torch.cuda.synchronize()
+    for b, (pk, out), (pk0, _, out0) in zip(bufs, res, alone):
+        b.check()
+        for k in ("packed_recv_count", "layout_range", "slot"):
+            eq(pk[k], bits(pk0[k]), k)
+        n = pk0["packed_recv_count"].cpu().numpy()
+        for d in range(R):
+            for l in range(E // R):
+                c = int(n[d, l])
+                eq(pk["packed_x"][d, l, :c], bits(pk0["packed_x"][d, l, :c]), "packed_x")
+        eq(out, bits(out0), "combine")
