@@ -9,12 +9,12 @@
 //  * low-latency BF16 combine (page "事件驱动 EP 内核的调度策略与零拷贝通信", section
 //    "低延迟模式": combine stays in BF16).
 //
-// One warp owns one token.  Lanes 0..K-1 read the token's top-k entries and
-// order them by (rank, k) (or by k for the low-latency mode); every lane then
-// owns 8 channels per step (one 16-byte vector per row), loads that vector
-// from each of the token's rows before accumulating (up to K 16-byte loads in
-// flight per lane), and reduces in fp32 with explicit fused multiply-adds in
-// the defined order.  The partial sums are never materialised: on one GPU a
+// One warp owns one token (or a channel slice of it).  Lanes 0..K-1 read the
+// token's top-k entries and order them by (rank, k) (or by k for the
+// low-latency mode); every lane then owns U vectors of 8 channels per step,
+// loads them from each of the token's rows before accumulating (up to U*K
+// 16-byte loads in flight per lane), and reduces in fp32 with explicit fused
+// multiply-adds in the defined order.  The partial sums are never materialised: on one GPU a
 // "partial" is the grouping of the sum.  Output: bf16, round to nearest even.
 #include <climits>
 #include <cstdlib>
@@ -47,8 +47,8 @@ __device__ __forceinline__ int4 f32x8_to_bf16(const float* f) {
 }
 
 // MODE 0: flat (rank partials), 1: hierarchical (rank, node, final), 2: low-latency (k order)
-template <int KMAX, int MODE>
-__global__ void __launch_bounds__(kCombineThreads, KMAX <= 8 ? (MODE == 2 ? 2 : 3) : 1) combine_kernel(CombineArgs a) {
+template <int KMAX, int MODE, int U>
+__global__ void __launch_bounds__(kCombineThreads, KMAX <= 8 ? (U == 2 ? 2 : 3) : 1) combine_kernel(CombineArgs a) {
     __shared__ int64_t sh_row[kCombineWarps][KMAX];
     __shared__ float sh_w[kCombineWarps][KMAX];
     __shared__ uint8_t sh_brk[kCombineWarps][KMAX];  // bit0: new rank group, bit1: new node group
@@ -145,97 +145,90 @@ __global__ void __launch_bounds__(kCombineThreads, KMAX <= 8 ? (MODE == 2 ? 2 : 
         __syncwarp();
         const uint8_t* y = static_cast<const uint8_t*>(a.y);
         int4* out = reinterpret_cast<int4*>(static_cast<uint8_t*>(a.out) + g * row_bytes);
-        // ---- channels ------------------------------------------------------------------
-        if (MODE == 2) {
-            // k order, one fp32 chain per channel: two vectors per lane per step,
-            // every load of the step issued before the first is used
-            for (int c = c_lo + lane; c < c_hi; c += 64) {
-                const bool two = c + 32 < c_hi;
-                int4 v0[KMAX], v1[KMAX];
+        // ---- channels: U vectors of 8 channels per lane per step, every load of
+        // the step issued before the first is used ----------------------------------
+        for (int c = c_lo + lane; c < c_hi; c += 32 * U) {
+            int4 v[U][KMAX];
 #pragma unroll
-                for (int j = 0; j < KMAX; ++j) {
-                    if (j < nvalid) {
-                        v0[j] = ld_nc_na_v4(y + roff[j] + (int64_t)c * 16);
-                        if (two) v1[j] = ld_nc_na_v4(y + roff[j] + (int64_t)(c + 32) * 16);
-                    }
-                }
-                float p0[8], p1[8];
+            for (int u = 0; u < U; ++u) {
+                const int cu = c + 32 * u;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) p0[i] = p1[i] = 0.0f;
-#pragma unroll
-                for (int j = 0; j < KMAX; ++j) {
-                    if (j < nvalid) {
-                        float yv[8];
-                        bf16x8_to_f32(v0[j], yv);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) p0[i] = __fmaf_rn(wr[j], yv[i], p0[i]);
-                        if (two) {
-                            bf16x8_to_f32(v1[j], yv);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) p1[i] = __fmaf_rn(wr[j], yv[i], p1[i]);
-                        }
-                    }
-                }
-                st_na_v4(out + c, f32x8_to_bf16(p0));
-                if (two) st_na_v4(out + c + 32, f32x8_to_bf16(p1));
+                for (int j = 0; j < KMAX; ++j)
+                    if (j < nvalid && cu < c_hi) v[u][j] = ld_nc_na_v4(y + roff[j] + (int64_t)cu * 16);
             }
-            continue;
-        }
-        for (int c = c_lo + lane; c < c_hi; c += 32) {
-            int4 v[KMAX];
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j)
-                if (j < nvalid) v[j] = ld_nc_na_v4(y + roff[j] + (int64_t)c * 16);
-            float fin[8], nod[8], par[8];
+            for (int u = 0; u < U; ++u) {
+                const int cu = c + 32 * u;
+                if (cu >= c_hi) break;
+                float fin[8], nod[8], par[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) fin[i] = nod[i] = par[i] = 0.0f;
+                for (int i = 0; i < 8; ++i) fin[i] = nod[i] = par[i] = 0.0f;
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j) {
-                if (j < nvalid) {
-                    if (MODE != 2 && j > 0 && (br[j] & 1)) {
+                for (int j = 0; j < KMAX; ++j) {
+                    if (j < nvalid) {
+                        if (MODE != 2 && j > 0 && (br[j] & 1)) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            if (MODE == 1) {
-                                nod[i] = __fadd_rn(nod[i], par[i]);
-                                if (br[j] & 2) {
-                                    fin[i] = __fadd_rn(fin[i], nod[i]);
-                                    nod[i] = 0.0f;
+                            for (int i = 0; i < 8; ++i) {
+                                if (MODE == 1) {
+                                    nod[i] = __fadd_rn(nod[i], par[i]);
+                                    if (br[j] & 2) {
+                                        fin[i] = __fadd_rn(fin[i], nod[i]);
+                                        nod[i] = 0.0f;
+                                    }
+                                } else {
+                                    fin[i] = __fadd_rn(fin[i], par[i]);
                                 }
-                            } else {
-                                fin[i] = __fadd_rn(fin[i], par[i]);
+                                par[i] = 0.0f;
                             }
-                            par[i] = 0.0f;
+                        }
+                        float yv[8];
+                        bf16x8_to_f32(v[u][j], yv);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) par[i] = __fmaf_rn(wr[j], yv[i], par[i]);
+                    }
+                }
+                if (nvalid > 0) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (MODE == 1) {
+                            nod[i] = __fadd_rn(nod[i], par[i]);
+                            fin[i] = __fadd_rn(fin[i], nod[i]);
+                        } else if (MODE == 0) {
+                            fin[i] = __fadd_rn(fin[i], par[i]);
+                        } else {
+                            fin[i] = par[i];
                         }
                     }
-                    float yv[8];
-                    bf16x8_to_f32(v[j], yv);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) par[i] = __fmaf_rn(wr[j], yv[i], par[i]);
                 }
+                st_na_v4(out + cu, f32x8_to_bf16(fin));
             }
-            if (nvalid > 0) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (MODE == 1) {
-                        nod[i] = __fadd_rn(nod[i], par[i]);
-                        fin[i] = __fadd_rn(fin[i], nod[i]);
-                    } else if (MODE == 0) {
-                        fin[i] = __fadd_rn(fin[i], par[i]);
-                    } else {
-                        fin[i] = par[i];
-                    }
-                }
-            }
-            st_na_v4(out + c, f32x8_to_bf16(fin));
         }
     }
 }
 
+// vectors per lane per step for K <= 8: 2 (16 loads of 16 B in flight per
+// lane at 2 CTAs/SM of registers) beat 1 (8 loads at 3 CTAs/SM) on GB300:
+// prefill combine 673 -> 649 us, hierarchical 2713 -> 2647 us.  Larger K
+// keeps 1 (the row arrays take the registers).
+static int combine_vectors(int mode) {
+    static const int forced = [] {  // EP_COMBINE_VEC: 1 or 2, for sweeps of the flat and staged modes
+        const char* v = getenv("EP_COMBINE_VEC");
+        return v ? atoi(v) : 0;
+    }();
+    if (mode != 2 && (forced == 1 || forced == 2)) return forced;
+    return 2;
+}
+
 template <int MODE>
-static cudaError_t launch_mode(const CombineArgs& a, int grid, cudaStream_t s) {
-    if (a.K <= 8) combine_kernel<8, MODE><<<grid, kCombineThreads, 0, s>>>(a);
-    else if (a.K <= 16) combine_kernel<16, MODE><<<grid, kCombineThreads, 0, s>>>(a);
-    else combine_kernel<32, MODE><<<grid, kCombineThreads, 0, s>>>(a);
+static cudaError_t launch_mode(const CombineArgs& a, int grid, int vec, cudaStream_t s) {
+    if (a.K <= 8) {
+        if (vec == 2) combine_kernel<8, MODE, 2><<<grid, kCombineThreads, 0, s>>>(a);
+        else combine_kernel<8, MODE, 1><<<grid, kCombineThreads, 0, s>>>(a);
+    } else if (a.K <= 16) {
+        combine_kernel<16, MODE, 1><<<grid, kCombineThreads, 0, s>>>(a);
+    } else {
+        combine_kernel<32, MODE, 1><<<grid, kCombineThreads, 0, s>>>(a);
+    }
     return cudaGetLastError();
 }
 
@@ -248,7 +241,8 @@ ep_status launch_combine(const CombineArgs& a, int mode, int num_sms, cudaStream
     // quarters of the resident warps an item (measured on the decode batch:
     // 1-2 slices 49 us, 7 slices 53 us, 8 slices 57 us).
     const int nvec = a.H / 8;
-    const int64_t conc = (int64_t)num_sms * (mode == 2 ? 2 : 3) * kCombineWarps;  // resident warps
+    const int vec = a.K <= 8 ? combine_vectors(mode) : 1;
+    const int64_t conc = (int64_t)num_sms * (vec == 2 ? 2 : 3) * kCombineWarps;  // resident warps
     int max_splits = nvec / 32 < 8 ? nvec / 32 : 8;
     if (max_splits < 1) max_splits = 1;
     int splits = max_splits;
@@ -268,7 +262,9 @@ ep_status launch_combine(const CombineArgs& a, int mode, int num_sms, cudaStream
     int64_t want = (items + kCombineWarps - 1) / kCombineWarps;
     const int64_t cap = (int64_t)num_sms * 16;
     const int grid = (int)(want < cap ? want : cap);
-    cudaError_t e = mode == 0 ? launch_mode<0>(b, grid, s) : mode == 1 ? launch_mode<1>(b, grid, s) : launch_mode<2>(b, grid, s);
+    cudaError_t e = mode == 0   ? launch_mode<0>(b, grid, vec, s)
+                    : mode == 1 ? launch_mode<1>(b, grid, vec, s)
+                                : launch_mode<2>(b, grid, vec, s);
     if (e != cudaSuccess) return cuda_error(e, "combine kernel");
     return EP_OK;
 }
