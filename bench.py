@@ -212,7 +212,7 @@ def run_ll_only(args):
     profiler on a small case: prints the per-kernel times, not the contract line."""
     import torch
     from combine_get_dispatch_histograms_gb300 import LLBuffer, inputs
-    dw = inputs.WORKLOADS["decode"]
+    dw = inputs.WORKLOADS[args.ll_workload]
     if args.ll_tokens:
         dw = dw.replace(T=args.ll_tokens, ll_cap=args.ll_tokens)
     if args.ll_experts:
@@ -226,22 +226,25 @@ def run_ll_only(args):
     out = torch.empty(dw.R, dw.T, dw.H, dtype=torch.bfloat16, device="cuda")
     st = torch.cuda.current_stream()
     times = []
+    mbs = [(t0, min(dw.ll_cap, dw.T - t0)) for t0 in range(0, dw.T, dw.ll_cap)]  # microbatches of <= cap tokens
     for i in range(args.warmup + args.steps):
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-        e[0].record(st)
-        buf.send(x, idxd, out=pk)
-        e[1].record(st)
-        buf.recv(pk)
-        e[2].record(st)
-        buf.combine(y, idxd, wd, pk, out=out)
-        e[3].record(st)
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            times.append([e[j].elapsed_time(e[j + 1]) * 1e3 for j in range(3)])
+        for t0, n in mbs:
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record(st)
+            buf.send(x, idxd, t0, n, out=pk)
+            e[1].record(st)
+            buf.recv(pk)
+            e[2].record(st)
+            buf.combine(y, idxd, wd, pk, t0, n, out=out)
+            e[3].record(st)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                times.append([e[j].elapsed_time(e[j + 1]) * 1e3 for j in range(3)])
     buf.check()
     med = [statistics.median(t[j] for t in times) for j in range(3)] if times else [None] * 3
-    print(json.dumps({"ll_only": {"R": dw.R, "T": dw.T, "H": dw.H, "cap": dw.ll_cap,
-                                  "send_us": med[0], "recv_us": med[1], "combine_us": med[2]}}), flush=True)
+    print(json.dumps({"ll_only": {"workload": dw.name, "R": dw.R, "T": dw.T, "H": dw.H, "cap": dw.ll_cap,
+                                  "microbatches": len(mbs), "send_us": med[0], "recv_us": med[1],
+                                  "combine_us": med[2], "per": "microbatch (median)"}}), flush=True)
     return 0
 
 
@@ -286,6 +289,8 @@ def main():
     ap.add_argument("--no-ll", action="store_true", help="skip the low-latency decode leg")
     ap.add_argument("--ll-only", action="store_true",
                     help="profiling mode: only the low-latency decode layer (no contract line)")
+    ap.add_argument("--ll-workload", default="decode", choices=["decode", "skewed"],
+                    help="with --ll-only: the low-latency workload (skewed runs 256-token microbatches)")
     ap.add_argument("--ll-tokens", type=int, default=0, help="with --ll-only: T = cap of the decode layer")
     ap.add_argument("--ll-experts", type=int, default=0,
                     help="with --ll-only: E of the decode layer (fewer experts: same messages, smaller buffers)")
