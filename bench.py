@@ -263,7 +263,10 @@ def run_reference(args, workload):
     cpu["value"] = value
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup,
+        # one whole step of the workload at the sampled rate (each timed step is a bounded sample)
+        "ms_per_step": round(1e3 * workload.R * workload.T / value, 1) if value else None,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload.name, "R": workload.R, "E": workload.E, "K": workload.K,
                    "T": workload.T, "H": workload.H},
