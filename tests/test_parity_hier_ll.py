@@ -81,6 +81,11 @@ def check_ll_microbatch(pk, sent, o_pk, R, E, K, T, H, cap, t0, n, idx):
     (8, 64, 8, 50, 256, 20, [(0, 20), (20, 20), (40, 10)], 0.05, 2),   # microbatches, ragged tail
     (2, 4, 2, 9, 384, 9, [(0, 9)], 0.3, 3),
     (4, 8, 2, 6, 128, 6, [(0, 0)], 0.0, 4),                             # empty microbatch
+    (1, 1, 1, 5, 128, 5, [(0, 5)], 0.0, 5),                             # one rank, one expert
+    (64, 64, 8, 4, 128, 4, [(0, 4)], 0.0, 6),                           # 64 ranks, one expert per rank
+    (4, 16, 16, 8, 16384, 8, [(0, 8)], 0.1, 7),                         # largest hidden, K = 16
+    (4, 8, 2, 3, 256, 1, [(0, 1), (1, 1), (2, 1)], 0.0, 8),             # cap 1: one token per microbatch
+    (2, 64, 32, 6, 256, 6, [(0, 6)], 0.0, 9),                           # K = 32
 ])
 def test_low_latency(R, E, K, T, H, cap, mbs, mask_p, seed):
     idx = inputs.random_topk(R, E, K, T, seed, mask_p)

@@ -24,6 +24,8 @@ CASES = [
     ("max-ranks-topk", (64, 128, 32, 40, 64, 8, 0.05, True, 9)),
     ("many-experts", (16, 4096, 8, 96, 64, 4, 0.0, True, 10)),
     ("more-channels-than-tokens", (4, 8, 2, 5, 64, 64, 0.0, True, 11)),
+    ("rows-in-chunks", (4, 16, 4, 50, 16384, 4, 0.1, True, 14)),       # 32 KB rows: several bulk chunks per row
+    ("ragged-chunk", (4, 8, 2, 40, 12296, 2, 0.0, True, 15)),          # last chunk of a row shorter
 ]
 
 
