@@ -80,3 +80,21 @@ def test_null_context_rejected(lib):
     assert lib.ep_get_dispatch_layout(None, None, None, None, None, None, None, None) == -1
     assert lib.ep_ctx_check(None, None) == -1
     assert lib.ep_ll_send(None, None, None, 0, 0, None, None) == -1
+
+
+def test_plain_c_caller(tmp_path):
+    """include/ep.h compiles as C and a C program links and calls the library."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not found")
+    lib_path = _lib.load()._name
+    exe = tmp_path / "abi_host"
+    src = os.path.join(ROOT, "tests", "c", "abi_host.c")
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), src,
+                        lib_path, f"-Wl,-rpath,{os.path.dirname(lib_path)}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and "c abi ok" in r.stdout, r.stdout + r.stderr
