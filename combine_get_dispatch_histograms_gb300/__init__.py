@@ -182,6 +182,23 @@ class Context:
         """wait=False: no host synchronisation (graph-capturable).  The row
         totals then stay on the device (handle["rank_base"][R], ["perm_rank_base"][R],
         ["stage_base"][R]) and the handle's num_*_rows are the worst-case bounds."""
+        return self._notify("ep_notify_dispatch", topk_idx, layout, stream, handle, wait)
+
+    def layout_notify(self, topk_idx: torch.Tensor, stream=None, handle: Optional[Handle] = None,
+                      out: Optional[dict] = None, wait: bool = True):
+        """get_dispatch_layout and notify_dispatch in two launches instead of
+        three; returns (layout dict, handle), the same as the two calls."""
+        _require_cuda(topk_idx)
+        R, E, T, N = self.R, self.E, self.T, self.N
+        lay = out if out is not None else dict(
+            num_tokens_per_expert=self._i32(R, E), num_tokens_per_rank=self._i32(R, R),
+            is_token_in_rank=torch.empty(R, T, R, dtype=torch.uint8, device=self.device))
+        if N > 1 and "num_tokens_per_node" not in lay:
+            lay["num_tokens_per_node"] = self._i32(R, N)
+            lay["is_token_in_node"] = torch.empty(R, T, N, dtype=torch.uint8, device=self.device)
+        return lay, self._notify("ep_layout_notify", topk_idx, lay, stream, handle, wait)
+
+    def _notify(self, fn: str, topk_idx, layout: dict, stream, handle: Optional[Handle], wait: bool) -> Handle:
         _require_cuda(topk_idx)
         h = handle if handle is not None else self.alloc_handle()
         cs = h.c_struct()
@@ -189,10 +206,12 @@ class Context:
             host_recv, host_exp, host_tot = self._host_recv, self._host_exp, self._host_tot
         else:
             host_recv = host_exp = host_tot = None
-        check("ep_notify_dispatch", self.lib.ep_notify_dispatch(
+        nodes = self.N > 1 or fn == "ep_notify_dispatch"
+        check(fn, getattr(self.lib, fn)(
             self._ctx, _ptr(topk_idx), _ptr(layout["num_tokens_per_expert"]), _ptr(layout["num_tokens_per_rank"]),
-            _ptr(layout["is_token_in_rank"]), _ptr(layout.get("num_tokens_per_node")),
-            _ptr(layout.get("is_token_in_node")), ctypes.byref(cs), host_recv, host_exp, host_tot, _stream(stream)))
+            _ptr(layout["is_token_in_rank"]), _ptr(layout.get("num_tokens_per_node") if nodes else None),
+            _ptr(layout.get("is_token_in_node") if nodes else None), ctypes.byref(cs), host_recv, host_exp, host_tot,
+            _stream(stream)))
         h.synced = wait
         if wait:
             h.host_num_recv_tokens = list(host_recv)

@@ -47,6 +47,7 @@ SIGNATURES = {
     "ep_get_dispatch_layout": (INT, [P, P, P, P, P, P, P, P]),
     "ep_get_dispatch_layout_noalloc": (INT, [I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P]),
     "ep_notify_dispatch": (INT, [P, P, P, P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, P]),
+    "ep_layout_notify": (INT, [P, P, P, P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, P]),
     "ep_dispatch": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, P, P, I64, P]),
     "ep_permute": (INT, [P, ctypes.POINTER(EpDispatchHandle), P, P, P, P, I64, P, P, I64, P]),
     "ep_dispatch_permuted": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, I64, P]),

@@ -61,14 +61,14 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // the last CTA of a source (completion counter) sums the partials of that
 // source into the outputs and re-arms the counter.  Integer sums do not
 // depend on the order, so the result is deterministic.
-__global__ void __launch_bounds__(kTileTokens)
-layout_kernel(const int64_t* __restrict__ topk_idx, int R, int E, int K, int T, int L, int N, int G,
-              TileGeom geom, int32_t* __restrict__ ntpe, int32_t* __restrict__ ntpr,
-              uint8_t* __restrict__ itir, int32_t* __restrict__ ntpn, uint8_t* __restrict__ itin,
-              int32_t* __restrict__ part, uint32_t* __restrict__ done, uint32_t* __restrict__ status) {
+// Returns true in the CTA that completed source s (it wrote the sums).
+__device__ bool layout_tile(const int64_t* __restrict__ topk_idx, int R, int E, int K, int T, int L, int N, int G,
+                            TileGeom geom, int32_t* __restrict__ ntpe, int32_t* __restrict__ ntpr,
+                            uint8_t* __restrict__ itir, int32_t* __restrict__ ntpn, uint8_t* __restrict__ itin,
+                            int32_t* __restrict__ part, uint32_t* __restrict__ done, uint32_t* __restrict__ status,
+                            int s, int tile) {
     extern __shared__ int32_t sh_cnt[];  // [E + R + N]
     __shared__ bool is_last;
-    const int s = blockIdx.y, tile = blockIdx.x;
     const int W = E + R + N;
     const int lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i < W; i += blockDim.x) sh_cnt[i] = 0;
@@ -125,7 +125,7 @@ layout_kernel(const int64_t* __restrict__ topk_idx, int R, int E, int K, int T, 
     __syncthreads();
     if (threadIdx.x == 0) is_last = (atomicAdd(&done[s], 1u) == (uint32_t)(geom.tiles_per_src - 1));
     __syncthreads();
-    if (!is_last) return;
+    if (!is_last) return false;
     __threadfence();
     const int32_t* first = part + (int64_t)s * geom.tiles_per_src * W;
     for (int i = threadIdx.x; i < W; i += blockDim.x) {
@@ -136,6 +136,16 @@ layout_kernel(const int64_t* __restrict__ topk_idx, int R, int E, int K, int T, 
         else ntpn[(int64_t)s * N + (i - E - R)] = acc;
     }
     if (threadIdx.x == 0) done[s] = 0;  // re-arm for the next call (stream ordered)
+    return true;
+}
+
+__global__ void __launch_bounds__(kTileTokens)
+layout_kernel(const int64_t* __restrict__ topk_idx, int R, int E, int K, int T, int L, int N, int G,
+              TileGeom geom, int32_t* __restrict__ ntpe, int32_t* __restrict__ ntpr,
+              uint8_t* __restrict__ itir, int32_t* __restrict__ ntpn, uint8_t* __restrict__ itin,
+              int32_t* __restrict__ part, uint32_t* __restrict__ done, uint32_t* __restrict__ status) {
+    layout_tile(topk_idx, R, E, K, T, L, N, G, geom, ntpe, ntpr, itir, ntpn, itin, part, done, status, blockIdx.y,
+                blockIdx.x);
 }
 
 // ============================================================================
@@ -350,6 +360,34 @@ __global__ void __launch_bounds__(kTileTokens) notify_count_kernel(NotifyArgs a)
     __syncthreads();
     int32_t* mine = a.part + ((int64_t)s * tiles + tile) * W;
     for (int i = threadIdx.x; i < W; i += blockDim.x) mine[i] = sh_cnt[i];
+}
+
+// ============================================================================
+// Layout fused with notify pass 1
+// ============================================================================
+// grid = (tiles_per_src, R).  Each CTA is a layout tile whose per-tile counts
+// (experts, receivers, nodes) are also notify's tile partials; the CTA that
+// completes a source writes the source's histograms, and the CTA that
+// completes the last source (a second completion counter) runs the global
+// scans.  One launch instead of layout + notify pass 1, nothing waits.
+__global__ void __launch_bounds__(kTileTokens) layout_notify_kernel(NotifyArgs a, int32_t* ntpe, int32_t* ntpr,
+                                                                   uint8_t* itir, int32_t* ntpn, uint8_t* itin,
+                                                                   uint32_t* done_src, uint32_t* done_all) {
+    extern __shared__ int32_t sh_dyn[];
+    __shared__ bool last_all;
+    if (!layout_tile(a.topk_idx, a.R, a.E, a.K, a.T, a.L, a.N, a.G, a.geom, ntpe, ntpr, itir, ntpn, itin, a.part,
+                     done_src, a.status, blockIdx.y, blockIdx.x))
+        return;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();  // this source's sums before the count
+        last_all = atomicAdd(done_all, 1u) == (uint32_t)(a.R - 1);
+    }
+    __syncthreads();
+    if (!last_all) return;
+    __threadfence();  // every source's sums are visible from here on
+    notify_global_scan(a, sh_dyn);
+    if (threadIdx.x == 0) *done_all = 0;  // re-arm for the next call (stream ordered)
 }
 
 // ============================================================================
@@ -730,11 +768,11 @@ extern "C" ep_status ep_get_dispatch_layout_noalloc(int32_t R, int32_t E, int32_
     return EP_OK;
 }
 
-extern "C" ep_status ep_notify_dispatch(ep_ctx* c, const int64_t* topk_idx, const int32_t* ntpe,
-                                        const int32_t* ntpr, const uint8_t* itir, const int32_t* ntpn,
-                                        const uint8_t* itin, const ep_dispatch_handle* h,
-                                        int32_t* host_num_recv, int32_t* host_num_recv_per_expert,
-                                        int32_t* host_totals, void* stream) {
+// Notify (and, with `fused`, the layout in the same launch as notify's first
+// pass: the layout pointers are then outputs).
+static ep_status notify_impl(ep_ctx* c, const int64_t* topk_idx, int32_t* ntpe, int32_t* ntpr, uint8_t* itir,
+                             int32_t* ntpn, uint8_t* itin, const ep_dispatch_handle* h, int32_t* host_num_recv,
+                             int32_t* host_num_recv_per_expert, int32_t* host_totals, void* stream, bool fused) {
     if (!c || !h) return set_error(EP_ERR_INVALID_ARG, "ctx or handle is NULL");
     c->last_launches = 0;
     const ep_config& f = c->cfg;
@@ -775,10 +813,19 @@ extern "C" ep_status ep_notify_dispatch(ep_ctx* c, const int64_t* topk_idx, cons
     a.epoch = ++c->notify_epoch;
     const int W = a.E + a.R + a.N;
     cudaStream_t s = as_stream(stream);
-    const int nblk = a.R * c->tiles.tiles_per_src + 1;
     const int Wscan = 2 * a.E + 3 * a.R + 98;
-    notify_count_kernel<<<nblk, kTileTokens, sizeof(int32_t) * (W > Wscan ? W : Wscan), s>>>(a);
-    EP_CHECK_LAUNCH("notify_count_kernel");
+    const size_t scan_smem = sizeof(int32_t) * (W > Wscan ? W : Wscan);
+    if (fused) {
+        dim3 lgrid(c->tiles.tiles_per_src, a.R);
+        layout_notify_kernel<<<lgrid, kTileTokens, scan_smem, s>>>(a, ntpe, ntpr, itir, hier ? ntpn : nullptr,
+                                                                   hier ? itin : nullptr, c->ws_layout_done,
+                                                                   c->ws_notify_done);
+        EP_CHECK_LAUNCH("layout_notify_kernel");
+    } else {
+        const int nblk = a.R * c->tiles.tiles_per_src + 1;
+        notify_count_kernel<<<nblk, kTileTokens, scan_smem, s>>>(a);
+        EP_CHECK_LAUNCH("notify_count_kernel");
+    }
     if (wait) EP_CUDA(cudaEventRecord(c->ev_counts, s));
     dim3 grid(c->tiles.tiles_per_src, a.R);
     notify_position_kernel<<<grid, kTileTokens, notify_position_smem(c), s>>>(a);
@@ -829,4 +876,27 @@ extern "C" ep_status ep_notify_dispatch(ep_ctx* c, const int64_t* topk_idx, cons
     const uint32_t flags = (uint32_t)hb[R + E + 3];
     if (flags & FLAG_INVALID_TOPK) return status_from_flags(flags);
     return EP_OK;
+}
+
+extern "C" ep_status ep_notify_dispatch(ep_ctx* c, const int64_t* topk_idx, const int32_t* ntpe,
+                                        const int32_t* ntpr, const uint8_t* itir, const int32_t* ntpn,
+                                        const uint8_t* itin, const ep_dispatch_handle* h,
+                                        int32_t* host_num_recv, int32_t* host_num_recv_per_expert,
+                                        int32_t* host_totals, void* stream) {
+    // the layout arrays are only read on this path
+    return notify_impl(c, topk_idx, const_cast<int32_t*>(ntpe), const_cast<int32_t*>(ntpr),
+                       const_cast<uint8_t*>(itir), const_cast<int32_t*>(ntpn), const_cast<uint8_t*>(itin), h,
+                       host_num_recv, host_num_recv_per_expert, host_totals, stream, false);
+}
+
+extern "C" ep_status ep_layout_notify(ep_ctx* c, const int64_t* topk_idx, int32_t* ntpe, int32_t* ntpr,
+                                      uint8_t* itir, int32_t* ntpn, uint8_t* itin, const ep_dispatch_handle* h,
+                                      int32_t* host_num_recv, int32_t* host_num_recv_per_expert,
+                                      int32_t* host_totals, void* stream) {
+    if (c && c->cfg.num_nodes > 1 && c->cfg.num_tokens > 0 && (!ntpn || !itin))
+        return set_error(EP_ERR_INVALID_ARG, "hierarchical mode needs the node layout outputs");
+    if (c && c->cfg.num_nodes == 1 && (ntpn || itin))
+        return set_error(EP_ERR_INVALID_ARG, "node layout outputs need num_nodes > 1");
+    return notify_impl(c, topk_idx, ntpe, ntpr, itir, ntpn, itin, h, host_num_recv, host_num_recv_per_expert,
+                       host_totals, stream, true);
 }

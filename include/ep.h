@@ -217,6 +217,20 @@ ep_status ep_notify_dispatch(ep_ctx* ctx, const int64_t* topk_idx,
                              const ep_dispatch_handle* handle, int32_t* host_num_recv_tokens,
                              int32_t* host_num_recv_per_expert, int32_t* host_totals, void* stream);
 
+/* Layout and notify together ([P2] DeepEP v2: the notify warps compute the
+ * layout on the fly instead of a separate get_dispatch_layout launch): the
+ * layout outputs of ep_get_dispatch_layout are written (num_tokens_per_node /
+ * is_token_in_node required iff N > 1, else NULL) and the handle is filled as
+ * by ep_notify_dispatch, in two kernel launches instead of three (one kernel
+ * computes the layout histograms, which are also notify's per-tile counts,
+ * and the CTA completing the last source runs the offset scans).  Same
+ * waiting and no-wait forms, same results. */
+ep_status ep_layout_notify(ep_ctx* ctx, const int64_t* topk_idx, int32_t* num_tokens_per_expert,
+                           int32_t* num_tokens_per_rank, uint8_t* is_token_in_rank,
+                           int32_t* num_tokens_per_node, uint8_t* is_token_in_node,
+                           const ep_dispatch_handle* handle, int32_t* host_num_recv_tokens,
+                           int32_t* host_num_recv_per_expert, int32_t* host_totals, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Dispatch scatter (v2 rank-level dedup) and local permute                 */
 /* ([P2] dispatch 过程, v2 direct 模式 "同一 destination rank 只发一份";           */
