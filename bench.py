@@ -467,9 +467,14 @@ def main():
             ctx.dispatch_permuted(x, idx_d, w_d, g_h, out=g_fused)
             ctx.combine(g_h, g_fused["permuted_x"], idx_d, w_d, out=g_out)
 
+        def nw_fewest():  # layout fused into notify, fused dispatch: four launches
+            ctx.layout_notify(idx_d, handle=g_h, out=g_lay, wait=False)
+            ctx.dispatch_permuted(x, idx_d, w_d, g_h, out=g_fused)
+            ctx.combine(g_h, g_fused["permuted_x"], idx_d, w_d, out=g_out)
+
         nw_graph = {"steps": "one CUDA graph per step: layout -> notify (no host wait) -> ... ; "
                           "worst-case buffers, row totals read on the device"}
-        for name, fn in (("step", nw_step), ("fused_path", nw_fused)):
+        for name, fn in (("step", nw_step), ("fused_path", nw_fused), ("fused_path_layout_in_notify", nw_fewest)):
             side = torch.cuda.Stream()
             side.wait_stream(stream)
             with torch.cuda.stream(side):
