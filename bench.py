@@ -847,7 +847,7 @@ def main():
                 "traffic_source": tr["source"] if tr else None}
 
     cpu = None
-    if not args.no_cpu:
+    if not args.no_cpu and world == 1:  # the CPU baseline is timed at N=1 only
         cpu = oracle_sample(w, budget_s=25.0, min_s=10.0)
         try:
             cpu["all_cores"] = oracle_parallel(w, 8.0)
