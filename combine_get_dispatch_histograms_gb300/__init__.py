@@ -320,6 +320,20 @@ class Context:
             _ptr(o["perm_src_token"]), _ptr(o.get("perm_weight")), o["permuted_xq"].shape[0], _stream(stream)))
         return o
 
+    def dispatch_permuted_quant(self, x, topk_idx, topk_weights, handle: Handle, stream=None, out=None) -> dict:
+        """Quantise the bf16 tokens and dispatch the FP8 rows into the permuted
+        layout in one pass (quantize_fp8 + dispatch_permuted_fp8 fused)."""
+        _require_cuda(x, topk_idx, topk_weights)
+        P = handle.num_perm_rows
+        o = out if out is not None else dict(
+            permuted_xq=torch.empty(P, self.fp8_row_bytes, dtype=torch.uint8, device=self.device),
+            perm_src_token=self._i32(P), perm_weight=torch.empty(P, dtype=torch.float32, device=self.device))
+        cs = handle.c_struct()
+        check("ep_dispatch_permuted_quant", self.lib.ep_dispatch_permuted_quant(
+            self._ctx, _ptr(x), _ptr(topk_idx), _ptr(topk_weights), ctypes.byref(cs), _ptr(o["permuted_xq"]),
+            _ptr(o["perm_src_token"]), _ptr(o.get("perm_weight")), o["permuted_xq"].shape[0], _stream(stream)))
+        return o
+
     # ---- combine ---------------------------------------------------------------
     def combine(self, handle: Handle, expert_out, topk_idx, topk_weights, stream=None, out=None, hier=False):
         _require_cuda(expert_out, topk_idx, topk_weights)

@@ -56,6 +56,7 @@ SIGNATURES = {
     "ep_dispatch_fp8": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, P, P, I64, P]),
     "ep_permute_fp8": (INT, [P, ctypes.POINTER(EpDispatchHandle), P, P, P, P, I64, P, P, I64, P]),
     "ep_dispatch_permuted_fp8": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, I64, P]),
+    "ep_dispatch_permuted_quant": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, I64, P]),
     "ep_combine": (INT, [P, ctypes.POINTER(EpDispatchHandle), P, I64, P, P, P, P]),
     "ep_dispatch_hier": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, I64, P, P, P, P, P, I64, P]),
     "ep_combine_hier": (INT, [P, ctypes.POINTER(EpDispatchHandle), P, I64, P, P, P, P]),

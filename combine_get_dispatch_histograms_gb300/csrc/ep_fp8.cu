@@ -42,6 +42,123 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __re
     }
 }
 
+// Quantise-and-scatter: the fused dispatch of FP8 rows straight from the bf16
+// tokens (one pass instead of ep_quantize_fp8 followed by
+// ep_dispatch_permuted_fp8; the same bytes come out).  Persistent CTAs own
+// contiguous token ranges; thread 0 streams the x rows global -> shared with
+// cp.async.bulk a few tokens ahead (one mbarrier per stage); all threads
+// quantise the staged row into an FP8 row in shared memory (two buffers);
+// thread 0 then writes that row to each of the token's permuted rows with
+// cp.async.bulk shared -> global, with the row's source token and weight.
+constexpr int kQsMaxStages = 8;
+
+struct QuantScatterArgs {
+    const uint16_t* x;         // [tokens][H] bf16
+    const int64_t* topk_idx;   // [tokens][K]
+    const float* w;            // [tokens][K]
+    const int32_t* perm_pos;   // [tokens][K]
+    uint8_t* out;              // [perm_rows][row_q]
+    int32_t* perm_src_token;   // [perm_rows]
+    float* perm_weight;        // [perm_rows] or NULL
+    int64_t tokens, perm_rows, row_q;
+    int K, H;
+    uint32_t* status;
+};
+
+__host__ __device__ inline size_t qs_fixed_smem() { return 128; }  // the stage mbarriers, padded
+
+__global__ void __launch_bounds__(256) quant_scatter_kernel(QuantScatterArgs a, int stages, int64_t timeout_ns) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    const int H = a.H, K = a.K;
+    const int64_t row_bytes = (int64_t)H * 2;
+    uint8_t* xs = smem + qs_fixed_smem();                  // [stages][row_bytes]
+    uint8_t* rows = xs + (size_t)stages * row_bytes;       // [2][row_q]
+    __shared__ int sh_abort;
+    const int64_t q0 = a.tokens * blockIdx.x / gridDim.x, q1 = a.tokens * (blockIdx.x + 1) / gridDim.x;
+    const int tid = threadIdx.x;
+    auto issue_load = [&](int64_t q) {
+        const int st = (int)((q - q0) % stages);
+        mbar_arrive_expect_tx(&bar[st], (uint32_t)row_bytes);
+        bulk_g2s(xs + (size_t)st * row_bytes, a.x + q * H, (uint32_t)row_bytes, &bar[st]);
+    };
+    int64_t next_load = q0;  // thread 0: first token whose load is not issued
+    if (tid == 0) {
+        for (int st = 0; st < stages; ++st) mbar_init(&bar[st], 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        for (; next_load < q1 && next_load < q0 + stages; ++next_load) issue_load(next_load);
+        sh_abort = 0;
+    }
+    int64_t q_stop = q1;
+    const int ngroups = H / 16;
+    for (int64_t q = q0; q < q1; ++q) {
+        const int64_t i = q - q0;
+        const int st = (int)(i % stages);
+        __syncthreads();  // thread 0 has seen the row buffer of token q-2 read out
+        if (!mbar_wait_bounded(&bar[st], (uint32_t)((i / stages) & 1), timeout_ns)) {
+            flag(a.status, FLAG_TIMEOUT);
+            atomicExch(&sh_abort, 1);
+        }
+        __syncthreads();
+        if (sh_abort) {
+            q_stop = q;
+            break;
+        }
+        uint8_t* row = rows + (size_t)(i & 1) * a.row_q;
+        const uint8_t* xrow = xs + (size_t)st * row_bytes;
+        for (int gi0 = 0; gi0 < ngroups; gi0 += blockDim.x) {
+            const int gi = gi0 + tid;
+            const bool act = gi < ngroups;
+            float v[16];
+            if (act) {
+                const int4 p0 = *reinterpret_cast<const int4*>(xrow + (size_t)gi * 32);
+                const int4 p1 = *reinterpret_cast<const int4*>(xrow + (size_t)gi * 32 + 16);
+                bf16x16_to_f32(p0, p1, v);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 16; ++u) v[u] = 0.0f;
+            }
+            float scale;
+            const int4 codes = quantize16(v, &scale);  // every lane takes part (shuffles)
+            if (act) {
+                *reinterpret_cast<int4*>(row + (size_t)gi * 16) = codes;
+                if ((gi & 7) == 0) *reinterpret_cast<float*>(row + H + (gi >> 3) * 4) = scale;
+            }
+        }
+        fence_proxy_async_smem();  // the row is read by the bulk copies below
+        __syncthreads();
+        if (tid == 0) {
+            for (int k = 0; k < K; ++k) {
+                const int32_t p = a.perm_pos[q * K + k];
+                if (p < 0) continue;
+                if (p >= a.perm_rows) {
+                    flag(a.status, FLAG_CAPACITY);
+                    continue;
+                }
+                bulk_s2g(a.out + (int64_t)p * a.row_q, row, (uint32_t)a.row_q);
+                a.perm_src_token[p] = (int32_t)q;
+                if (a.perm_weight) a.perm_weight[p] = a.w[q * K + k];
+            }
+            bulk_commit();
+            // the x stage of this token is free: stream the token `stages` ahead
+            if (next_load < q1) {
+                fence_proxy_async_smem();
+                issue_load(next_load);
+                ++next_load;
+            }
+            // the row buffer of the previous token must be read out before reuse
+            bulk_wait_read<1>();
+        }
+    }
+    if (tid == 0) {
+        bulk_wait_all();
+        // after an aborted wait, let the loads still in flight land before leaving
+        for (int64_t qq = q_stop; qq < next_load; ++qq)
+            mbar_wait_bounded(&bar[(qq - q0) % stages], (uint32_t)(((qq - q0) / stages) & 1), timeout_ns);
+    }
+}
+
 }  // namespace ep
 
 using namespace ep;
@@ -100,4 +217,55 @@ extern "C" ep_status ep_dispatch_permuted_fp8(ep_ctx* c, const uint8_t* xq, cons
     if (st != EP_OK) return st;
     return dispatch_permuted_rows(c, xq, fp8_row_bytes(c->cfg.hidden), topk_idx, topk_weights, h, permuted_xq,
                                   perm_src_token, perm_weight, perm_capacity_rows, stream);
+}
+
+extern "C" ep_status ep_dispatch_permuted_quant(ep_ctx* c, const void* x, const int64_t* topk_idx,
+                                                const float* topk_weights, const ep_dispatch_handle* h,
+                                                uint8_t* permuted_xq, int32_t* perm_src_token, float* perm_weight,
+                                                int64_t perm_capacity_rows, void* stream) {
+    ep_status st = fp8_ok(c);
+    if (st != EP_OK) return st;
+    if (!h) return set_error(EP_ERR_INVALID_ARG, "handle is NULL");
+    c->last_launches = 0;
+    const ep_config& f = c->cfg;
+    if (f.num_tokens == 0 || (c->totals_known && c->last_total_perm == 0) || perm_capacity_rows == 0) return EP_OK;
+    if (!x || !aligned16(x) || !permuted_xq || !aligned16(permuted_xq))
+        return set_error(EP_ERR_INVALID_ARG, "x and permuted_xq must be 16-byte aligned");
+    if (!topk_idx || !h->perm_pos || !perm_src_token || (perm_weight && !topk_weights))
+        return set_error(EP_ERR_INVALID_ARG, "NULL fused dispatch argument");
+    if (c->totals_known && perm_capacity_rows < c->last_total_perm)
+        return set_error(EP_ERR_CAPACITY, "permuted buffers hold %lld rows, notify counted %lld",
+                         (long long)perm_capacity_rows, (long long)c->last_total_perm);
+    QuantScatterArgs a;
+    a.x = static_cast<const uint16_t*>(x);
+    a.topk_idx = topk_idx;
+    a.w = topk_weights;
+    a.perm_pos = h->perm_pos;
+    a.out = permuted_xq;
+    a.perm_src_token = perm_src_token;
+    a.perm_weight = perm_weight;
+    a.tokens = (int64_t)f.num_ranks * f.num_tokens;
+    a.perm_rows = perm_capacity_rows;
+    a.row_q = fp8_row_bytes(f.hidden);
+    a.K = f.num_topk;
+    a.H = f.hidden;
+    a.status = c->status;
+    // three CTAs per SM, ~72 KB each: two FP8 row buffers and as many staged x rows as fit
+    const int64_t row_bytes = (int64_t)f.hidden * 2;
+    const size_t budget = 72 * 1024;
+    int stages = (int)((budget - qs_fixed_smem() - 2 * (size_t)a.row_q) / (size_t)row_bytes);
+    if (stages > kQsMaxStages) stages = kQsMaxStages;
+    if (stages < 2) stages = 2;
+    const size_t smem = qs_fixed_smem() + (size_t)stages * row_bytes + 2 * (size_t)a.row_q;
+    static int raised[kMaxDevicesTracked] = {};
+    if (c->device < 0 || c->device >= kMaxDevicesTracked || raised[c->device] < (int)smem) {
+        EP_CUDA(cudaFuncSetAttribute(quant_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        if (c->device >= 0 && c->device < kMaxDevicesTracked) raised[c->device] = (int)smem;
+    }
+    int64_t grid = (int64_t)c->num_sms * 3;
+    if (grid > a.tokens) grid = a.tokens;
+    quant_scatter_kernel<<<(int)grid, 256, smem, as_stream(stream)>>>(a, stages, c->wait_timeout_ns);
+    EP_CHECK_LAUNCH("quant_scatter_kernel");
+    c->last_launches = 1;
+    return EP_OK;
 }

@@ -304,6 +304,18 @@ ep_status ep_dispatch_permuted_fp8(ep_ctx* ctx, const uint8_t* xq, const int64_t
                                    uint8_t* permuted_xq, int32_t* perm_src_token, float* perm_weight,
                                    int64_t perm_capacity_rows, void* stream);
 
+/* Quantise and dispatch in one pass: the bf16 tokens x [R][T][H] are
+ * quantised (the rule of ep_quantize_fp8) and each FP8 row written straight
+ * into its permuted rows ([P1] 低延迟模式: FP8 conversion fused into the send;
+ * here for the normal path's expert-major layout).  permuted_xq,
+ * perm_src_token and perm_weight equal those of ep_quantize_fp8 followed by
+ * ep_dispatch_permuted_fp8 (padding bytes of a row excepted), without the
+ * intermediate [R*T] FP8 rows. */
+ep_status ep_dispatch_permuted_quant(ep_ctx* ctx, const void* x, const int64_t* topk_idx,
+                                     const float* topk_weights, const ep_dispatch_handle* handle,
+                                     uint8_t* permuted_xq, int32_t* perm_src_token, float* perm_weight,
+                                     int64_t perm_capacity_rows, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Combine ([P2] combine 过程; v2 "rank-level partial result ... epilogue 按    */
 /* 不同 destination rank 做最终归约")                                             */

@@ -121,3 +121,54 @@ def test_quantize_every_bf16_value_for_many_scales():
     buf.check()
     eq(pk["packed_x"][0, 0, :T], o_rows[:, :H], "LL message codes (exhaustive bf16 x)")
     eq(pk["packed_scales"][0, 0, :T], o_rows[:, H:].view(np.float32), "LL message scales")
+
+
+@pytest.mark.parametrize("R,E,K,T,H,C,mask_p,align,seed,wait", [
+    (4, 8, 2, 16, 128, 2, 0.0, 1, 0, True),
+    (8, 64, 8, 300, 512, 4, 0.05, 1, 1, True),
+    (4, 16, 4, 77, 384, 3, 0.2, 1, 2, True),
+    (8, 256, 8, 200, 7168, 8, 0.0, 1, 3, True),      # the prefill row size
+    (4, 16, 4, 150, 256, 4, 0.1, 16, 4, True),       # expert-aligned blocks
+    (4, 16, 4, 150, 256, 4, 0.1, 1, 5, False),       # no-wait notify, worst-case buffers
+    (4, 8, 2, 0, 128, 2, 0.0, 1, 6, True),           # no tokens
+])
+def test_quantise_and_dispatch_in_one_pass(R, E, K, T, H, C, mask_p, align, seed, wait):
+    """ep_dispatch_permuted_quant gives the bytes of quantize_fp8 followed by
+    dispatch_permuted_fp8, and the oracle's FP8 rows in the oracle's order."""
+    idx = inputs.random_topk(R, E, K, T, seed, mask_p)
+    x = inputs.random_x(R, T, H, seed)
+    if seed == 1:
+        x[0, 3] = 0.0
+    w = inputs.random_weights(R, T, K, seed)
+    ctx = Context(R, E, K, T, H, num_channels=C, expert_alignment=align)
+    xd, idxd, wd = x.cuda(), idx.cuda(), w.cuda()
+    lay = ctx.get_dispatch_layout(idxd)
+    h = ctx.notify_dispatch(idxd, lay, wait=wait)
+    one = ctx.dispatch_permuted_quant(xd, idxd, wd, h)
+    ctx.check()
+    rq = ctx.fp8_row_bytes
+    n_def = H + H // 32
+    o_note = orc.notify(orc.layout(idx, R, E), R, E, T, C, align=align)
+    P = int(o_note["perm_rank_base"][R])
+    o_rows = _oracle_rows(x, rq)
+    pp = h["perm_pos"].cpu().numpy()
+    eq(pp, orc.permute(idx, np.zeros((int(o_note["rank_base"][R]), 8), np.uint16), o_note, R, E)["perm_pos"],
+       "perm_pos")
+    got = bits(one["permuted_xq"])[:P]
+    tok = bits(one["perm_src_token"])[:P]
+    wgt = bits(one["perm_weight"])[:P]
+    wn = w.numpy()
+    for s_, t_, k_ in zip(*np.nonzero(pp >= 0)):
+        r = pp[s_, t_, k_]
+        assert tok[r] == s_ * T + t_
+        assert wgt[r] == wn[s_, t_, k_]
+        eq(got[r, :n_def], o_rows[s_ * T + t_, :n_def], f"row {r}")
+    if T > 0 and wait:
+        # byte for byte the two-pass form
+        xq = ctx.quantize_fp8(xd)
+        two = ctx.dispatch_permuted_fp8(xq, idxd, wd, h)
+        ctx.check()
+        used = np.zeros(P, bool)
+        used[pp[pp >= 0]] = True
+        eq(got[used][:, :n_def], bits(two["permuted_xq"])[:P][used][:, :n_def], "one pass vs two passes")
+        eq(tok[used], bits(two["perm_src_token"])[:P][used], "perm_src_token")
