@@ -320,6 +320,22 @@ class Context:
             _ptr(o["perm_src_token"]), _ptr(o.get("perm_weight")), o["permuted_xq"].shape[0], _stream(stream)))
         return o
 
+    def dispatch_quant(self, x, topk_idx, topk_weights, handle: Handle, stream=None, out=None) -> dict:
+        """Quantise the bf16 tokens and scatter the FP8 rows to the receive
+        layout in one pass (quantize_fp8 + dispatch_fp8 fused)."""
+        _require_cuda(x, topk_idx, topk_weights)
+        rows = handle.num_recv_rows
+        o = out if out is not None else dict(
+            recv_xq=torch.empty(rows, self.fp8_row_bytes, dtype=torch.uint8, device=self.device),
+            recv_src_rank=self._i32(rows), recv_src_idx=self._i32(rows), recv_topk_idx=self._i32(rows, self.K),
+            recv_topk_weights=torch.empty(rows, self.K, dtype=torch.float32, device=self.device))
+        cs = handle.c_struct()
+        check("ep_dispatch_quant", self.lib.ep_dispatch_quant(
+            self._ctx, _ptr(x), _ptr(topk_idx), _ptr(topk_weights), ctypes.byref(cs), _ptr(o["recv_xq"]),
+            _ptr(o["recv_src_rank"]), _ptr(o["recv_src_idx"]), _ptr(o["recv_topk_idx"]),
+            _ptr(o["recv_topk_weights"]), o["recv_xq"].shape[0], _stream(stream)))
+        return o
+
     def dispatch_permuted_quant(self, x, topk_idx, topk_weights, handle: Handle, stream=None, out=None) -> dict:
         """Quantise the bf16 tokens and dispatch the FP8 rows into the permuted
         layout in one pass (quantize_fp8 + dispatch_permuted_fp8 fused)."""

@@ -54,6 +54,7 @@ SIGNATURES = {
     "ep_fp8_row_bytes": (I64, [INT]),
     "ep_quantize_fp8": (INT, [P, P, P, P]),
     "ep_dispatch_fp8": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, P, P, I64, P]),
+    "ep_dispatch_quant": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, P, P, I64, P]),
     "ep_permute_fp8": (INT, [P, ctypes.POINTER(EpDispatchHandle), P, P, P, P, I64, P, P, I64, P]),
     "ep_dispatch_permuted_fp8": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, I64, P]),
     "ep_dispatch_permuted_quant": (INT, [P, P, P, P, ctypes.POINTER(EpDispatchHandle), P, P, P, I64, P]),

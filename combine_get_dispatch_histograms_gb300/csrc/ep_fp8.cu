@@ -56,17 +56,26 @@ struct QuantScatterArgs {
     const uint16_t* x;         // [tokens][H] bf16
     const int64_t* topk_idx;   // [tokens][K]
     const float* w;            // [tokens][K]
+    // permuted destinations
     const int32_t* perm_pos;   // [tokens][K]
-    uint8_t* out;              // [perm_rows][row_q]
-    int32_t* perm_src_token;   // [perm_rows]
-    float* perm_weight;        // [perm_rows] or NULL
-    int64_t tokens, perm_rows, row_q;
-    int K, H;
+    int32_t* perm_src_token;   // [rows]
+    float* perm_weight;        // [rows] or NULL
+    // per-rank destinations (the dispatch scatter's receive layout)
+    const int32_t* send_pos;   // [tokens][R]
+    const int32_t* rank_base;  // [R+1]
+    int32_t* recv_src_rank;    // [rows]
+    int32_t* recv_src_idx;     // [rows]
+    int32_t* recv_topk_idx;    // [rows][K]
+    float* recv_topk_w;        // [rows][K]
+    uint8_t* out;              // [rows][row_q]
+    int64_t tokens, rows, row_q;
+    int K, H, R, T, L;
     uint32_t* status;
 };
 
 __host__ __device__ inline size_t qs_fixed_smem() { return 128; }  // the stage mbarriers, padded
 
+template <bool kRecv>
 __global__ void __launch_bounds__(256) quant_scatter_kernel(QuantScatterArgs a, int stages, int64_t timeout_ns) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
@@ -75,6 +84,9 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(QuantScatterArgs a, 
     uint8_t* xs = smem + qs_fixed_smem();                  // [stages][row_bytes]
     uint8_t* rows = xs + (size_t)stages * row_bytes;       // [2][row_q]
     __shared__ int sh_abort;
+    __shared__ int64_t sh_dst[kRecv ? kMaxRanks : kMaxTopk];  // row per destination, -1 if none
+    __shared__ int64_t sh_e[kMaxTopk];                             // the token's top-k entries
+    __shared__ float sh_w[kMaxTopk];
     const int64_t q0 = a.tokens * blockIdx.x / gridDim.x, q1 = a.tokens * (blockIdx.x + 1) / gridDim.x;
     const int tid = threadIdx.x;
     auto issue_load = [&](int64_t q) {
@@ -107,6 +119,19 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(QuantScatterArgs a, 
         }
         uint8_t* row = rows + (size_t)(i & 1) * a.row_q;
         const uint8_t* xrow = xs + (size_t)st * row_bytes;
+        // this token's routing, loaded now and kept until after the quantisation
+        // (the loads' latency hides behind it)
+        int64_t my_e = -1;
+        float my_w = 0.0f;
+        int32_t my_pos = -1;
+        if (tid < K) {
+            my_e = a.topk_idx[q * K + tid];
+            my_w = a.w[q * K + tid];
+            if constexpr (!kRecv) my_pos = a.perm_pos[q * K + tid];
+        }
+        if constexpr (kRecv) {
+            if (tid >= 32 && tid - 32 < a.R) my_pos = a.send_pos[q * a.R + (tid - 32)];
+        }
         for (int gi0 = 0; gi0 < ngroups; gi0 += blockDim.x) {
             const int gi = gi0 + tid;
             const bool act = gi < ngroups;
@@ -126,20 +151,61 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(QuantScatterArgs a, 
                 if ((gi & 7) == 0) *reinterpret_cast<float*>(row + H + (gi >> 3) * 4) = scale;
             }
         }
+        if (tid < K) {
+            sh_e[tid] = my_e;
+            sh_w[tid] = my_w;
+        }
+        if constexpr (kRecv) {
+            // threads 32..32+R-1: one destination rank each, its receive row
+            if (tid >= 32 && tid - 32 < a.R) {
+                int64_t r = -1;
+                if (my_pos >= 0) {
+                    r = (int64_t)a.rank_base[tid - 32] + my_pos;
+                    if (r >= a.rows) {
+                        flag(a.status, FLAG_CAPACITY);
+                        r = -1;
+                    }
+                }
+                sh_dst[tid - 32] = r;
+            }
+        } else {
+            // threads 0..K-1: one top-k entry each, its permuted row and metadata
+            if (tid < K) {
+                int64_t p = my_pos;
+                if (p >= a.rows) {
+                    flag(a.status, FLAG_CAPACITY);
+                    p = -1;
+                }
+                if (p >= 0) {
+                    a.perm_src_token[p] = (int32_t)q;
+                    if (a.perm_weight) a.perm_weight[p] = my_w;
+                }
+                sh_dst[tid] = p;
+            }
+        }
         fence_proxy_async_smem();  // the row is read by the bulk copies below
         __syncthreads();
-        if (tid == 0) {
-            for (int k = 0; k < K; ++k) {
-                const int32_t p = a.perm_pos[q * K + k];
-                if (p < 0) continue;
-                if (p >= a.perm_rows) {
-                    flag(a.status, FLAG_CAPACITY);
-                    continue;
+        if constexpr (kRecv) {
+            // the receive rows' metadata: thread 32 + d for destination d
+            if (tid >= 32 && tid - 32 < a.R) {
+                const int d = tid - 32;
+                const int64_t r = sh_dst[d];
+                if (r >= 0) {
+                    a.recv_src_rank[r] = (int32_t)(q / a.T);
+                    a.recv_src_idx[r] = (int32_t)(q % a.T);
+                    for (int k = 0; k < K; ++k) {
+                        const int64_t e = sh_e[k];
+                        const bool on = e >= 0 && e / a.L == d;
+                        a.recv_topk_idx[r * K + k] = on ? (int32_t)(e - (int64_t)d * a.L) : -1;
+                        a.recv_topk_w[r * K + k] = on ? sh_w[k] : 0.0f;
+                    }
                 }
-                bulk_s2g(a.out + (int64_t)p * a.row_q, row, (uint32_t)a.row_q);
-                a.perm_src_token[p] = (int32_t)q;
-                if (a.perm_weight) a.perm_weight[p] = a.w[q * K + k];
             }
+        }
+        if (tid == 0) {
+            const int nd = kRecv ? a.R : K;
+            for (int j = 0; j < nd; ++j)
+                if (sh_dst[j] >= 0) bulk_s2g(a.out + sh_dst[j] * a.row_q, row, (uint32_t)a.row_q);
             bulk_commit();
             // the x stage of this token is free: stream the token `stages` ahead
             if (next_load < q1) {
@@ -219,6 +285,49 @@ extern "C" ep_status ep_dispatch_permuted_fp8(ep_ctx* c, const uint8_t* xq, cons
                                   perm_src_token, perm_weight, perm_capacity_rows, stream);
 }
 
+template <bool kRecv>
+static ep_status launch_quant_scatter(ep_ctx* c, const QuantScatterArgs& a, void* stream) {
+    // three CTAs per SM, ~72 KB each: two FP8 row buffers and as many staged x rows as fit
+    const int64_t row_bytes = (int64_t)a.H * 2;
+    const size_t budget = 72 * 1024;
+    int stages = (int)((budget - qs_fixed_smem() - 2 * (size_t)a.row_q) / (size_t)row_bytes);
+    if (stages > kQsMaxStages) stages = kQsMaxStages;
+    if (stages < 2) stages = 2;
+    const size_t smem = qs_fixed_smem() + (size_t)stages * row_bytes + 2 * (size_t)a.row_q;
+    static int raised[kMaxDevicesTracked] = {};
+    if (c->device < 0 || c->device >= kMaxDevicesTracked || raised[c->device] < (int)smem) {
+        EP_CUDA(cudaFuncSetAttribute(quant_scatter_kernel<kRecv>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem));
+        if (c->device >= 0 && c->device < kMaxDevicesTracked) raised[c->device] = (int)smem;
+    }
+    int64_t grid = (int64_t)c->num_sms * 3;
+    if (grid > a.tokens) grid = a.tokens;
+    quant_scatter_kernel<kRecv><<<(int)grid, 256, smem, as_stream(stream)>>>(a, stages, c->wait_timeout_ns);
+    EP_CHECK_LAUNCH("quant_scatter_kernel");
+    c->last_launches = 1;
+    return EP_OK;
+}
+
+static QuantScatterArgs quant_args(const ep_ctx* c, const void* x, const int64_t* topk_idx, const float* w,
+                                   uint8_t* out, int64_t rows) {
+    const ep_config& f = c->cfg;
+    QuantScatterArgs a{};
+    a.x = static_cast<const uint16_t*>(x);
+    a.topk_idx = topk_idx;
+    a.w = w;
+    a.out = out;
+    a.tokens = (int64_t)f.num_ranks * f.num_tokens;
+    a.rows = rows;
+    a.row_q = fp8_row_bytes(f.hidden);
+    a.K = f.num_topk;
+    a.H = f.hidden;
+    a.R = f.num_ranks;
+    a.T = f.num_tokens;
+    a.L = c->L;
+    a.status = c->status;
+    return a;
+}
+
 extern "C" ep_status ep_dispatch_permuted_quant(ep_ctx* c, const void* x, const int64_t* topk_idx,
                                                 const float* topk_weights, const ep_dispatch_handle* h,
                                                 uint8_t* permuted_xq, int32_t* perm_src_token, float* perm_weight,
@@ -236,36 +345,37 @@ extern "C" ep_status ep_dispatch_permuted_quant(ep_ctx* c, const void* x, const 
     if (c->totals_known && perm_capacity_rows < c->last_total_perm)
         return set_error(EP_ERR_CAPACITY, "permuted buffers hold %lld rows, notify counted %lld",
                          (long long)perm_capacity_rows, (long long)c->last_total_perm);
-    QuantScatterArgs a;
-    a.x = static_cast<const uint16_t*>(x);
-    a.topk_idx = topk_idx;
-    a.w = topk_weights;
+    QuantScatterArgs a = quant_args(c, x, topk_idx, topk_weights, permuted_xq, perm_capacity_rows);
     a.perm_pos = h->perm_pos;
-    a.out = permuted_xq;
     a.perm_src_token = perm_src_token;
     a.perm_weight = perm_weight;
-    a.tokens = (int64_t)f.num_ranks * f.num_tokens;
-    a.perm_rows = perm_capacity_rows;
-    a.row_q = fp8_row_bytes(f.hidden);
-    a.K = f.num_topk;
-    a.H = f.hidden;
-    a.status = c->status;
-    // three CTAs per SM, ~72 KB each: two FP8 row buffers and as many staged x rows as fit
-    const int64_t row_bytes = (int64_t)f.hidden * 2;
-    const size_t budget = 72 * 1024;
-    int stages = (int)((budget - qs_fixed_smem() - 2 * (size_t)a.row_q) / (size_t)row_bytes);
-    if (stages > kQsMaxStages) stages = kQsMaxStages;
-    if (stages < 2) stages = 2;
-    const size_t smem = qs_fixed_smem() + (size_t)stages * row_bytes + 2 * (size_t)a.row_q;
-    static int raised[kMaxDevicesTracked] = {};
-    if (c->device < 0 || c->device >= kMaxDevicesTracked || raised[c->device] < (int)smem) {
-        EP_CUDA(cudaFuncSetAttribute(quant_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        if (c->device >= 0 && c->device < kMaxDevicesTracked) raised[c->device] = (int)smem;
-    }
-    int64_t grid = (int64_t)c->num_sms * 3;
-    if (grid > a.tokens) grid = a.tokens;
-    quant_scatter_kernel<<<(int)grid, 256, smem, as_stream(stream)>>>(a, stages, c->wait_timeout_ns);
-    EP_CHECK_LAUNCH("quant_scatter_kernel");
-    c->last_launches = 1;
-    return EP_OK;
+    return launch_quant_scatter<false>(c, a, stream);
+}
+
+extern "C" ep_status ep_dispatch_quant(ep_ctx* c, const void* x, const int64_t* topk_idx, const float* topk_weights,
+                                       const ep_dispatch_handle* h, uint8_t* recv_xq, int32_t* recv_src_rank,
+                                       int32_t* recv_src_idx, int32_t* recv_topk_idx, float* recv_topk_weights,
+                                       int64_t recv_capacity_rows, void* stream) {
+    ep_status st = fp8_ok(c);
+    if (st != EP_OK) return st;
+    if (!h) return set_error(EP_ERR_INVALID_ARG, "handle is NULL");
+    c->last_launches = 0;
+    const ep_config& f = c->cfg;
+    if (f.num_tokens == 0 || (c->totals_known && c->last_total_recv == 0) || recv_capacity_rows == 0) return EP_OK;
+    if (!x || !aligned16(x) || !recv_xq || !aligned16(recv_xq))
+        return set_error(EP_ERR_INVALID_ARG, "x and recv_xq must be 16-byte aligned");
+    if (!topk_idx || !topk_weights || !h->send_pos || !h->rank_base || !recv_src_rank || !recv_src_idx ||
+        !recv_topk_idx || !recv_topk_weights)
+        return set_error(EP_ERR_INVALID_ARG, "NULL dispatch argument");
+    if (c->totals_known && recv_capacity_rows < c->last_total_recv)
+        return set_error(EP_ERR_CAPACITY, "recv buffers hold %lld rows, notify counted %lld",
+                         (long long)recv_capacity_rows, (long long)c->last_total_recv);
+    QuantScatterArgs a = quant_args(c, x, topk_idx, topk_weights, recv_xq, recv_capacity_rows);
+    a.send_pos = h->send_pos;
+    a.rank_base = h->rank_base;
+    a.recv_src_rank = recv_src_rank;
+    a.recv_src_idx = recv_src_idx;
+    a.recv_topk_idx = recv_topk_idx;
+    a.recv_topk_w = recv_topk_weights;
+    return launch_quant_scatter<true>(c, a, stream);
 }

@@ -315,6 +315,13 @@ ep_status ep_dispatch_permuted_quant(ep_ctx* ctx, const void* x, const int64_t* 
                                      const float* topk_weights, const ep_dispatch_handle* handle,
                                      uint8_t* permuted_xq, int32_t* perm_src_token, float* perm_weight,
                                      int64_t perm_capacity_rows, void* stream);
+/* The same for the dispatch scatter's receive layout: recv_xq (FP8 rows) and
+ * the recv_* metadata equal those of ep_quantize_fp8 followed by
+ * ep_dispatch_fp8. */
+ep_status ep_dispatch_quant(ep_ctx* ctx, const void* x, const int64_t* topk_idx, const float* topk_weights,
+                            const ep_dispatch_handle* handle, uint8_t* recv_xq, int32_t* recv_src_rank,
+                            int32_t* recv_src_idx, int32_t* recv_topk_idx, float* recv_topk_weights,
+                            int64_t recv_capacity_rows, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Combine ([P2] combine 过程; v2 "rank-level partial result ... epilogue 按    */

@@ -172,3 +172,42 @@ def test_quantise_and_dispatch_in_one_pass(R, E, K, T, H, C, mask_p, align, seed
         used[pp[pp >= 0]] = True
         eq(got[used][:, :n_def], bits(two["permuted_xq"])[:P][used][:, :n_def], "one pass vs two passes")
         eq(tok[used], bits(two["perm_src_token"])[:P][used], "perm_src_token")
+
+
+@pytest.mark.parametrize("R,E,K,T,H,C,mask_p,seed,wait", [
+    (4, 8, 2, 16, 128, 2, 0.0, 0, True),
+    (8, 64, 8, 300, 512, 4, 0.05, 1, True),
+    (16, 256, 8, 100, 7168, 8, 0.1, 2, True),
+    (4, 16, 4, 150, 256, 4, 0.1, 3, False),        # no-wait notify, worst-case buffers
+    (4, 8, 2, 0, 128, 2, 0.0, 4, True),            # no tokens
+])
+def test_quantise_and_scatter_in_one_pass(R, E, K, T, H, C, mask_p, seed, wait):
+    """ep_dispatch_quant: the receive layout of quantize_fp8 + dispatch_fp8, and
+    the oracle's metadata and FP8 rows."""
+    idx = inputs.random_topk(R, E, K, T, seed, mask_p)
+    x = inputs.random_x(R, T, H, seed)
+    w = inputs.random_weights(R, T, K, seed)
+    ctx = Context(R, E, K, T, H, num_channels=C)
+    xd, idxd, wd = x.cuda(), idx.cuda(), w.cuda()
+    h = ctx.notify_dispatch(idxd, ctx.get_dispatch_layout(idxd), wait=wait)
+    one = ctx.dispatch_quant(xd, idxd, wd, h, out=None if wait else ctx_recv_fp8(ctx))
+    ctx.check()
+    rq = ctx.fp8_row_bytes
+    n_def = H + H // 32
+    o_note = orc.notify(orc.layout(idx, R, E), R, E, T, C)
+    nr = int(o_note["rank_base"][R])
+    o_rows = _oracle_rows(x, rq)
+    rows16 = o_rows.view(np.uint16).reshape(R, T, rq // 2) if T > 0 else np.zeros((R, 0, rq // 2), np.uint16)
+    o_disp = orc.dispatch(rows16, idx, w, o_note, R, E)
+    for k in ("recv_src_rank", "recv_src_idx", "recv_topk_idx", "recv_topk_weights"):
+        eq(bits(one[k])[:nr], o_disp[k], k)
+    eq(bits(one["recv_xq"])[:nr, :n_def], o_disp["recv_x"].view(np.uint8)[:, :n_def], "recv FP8 rows")
+
+
+def ctx_recv_fp8(ctx):
+    rows = ctx.max_rows[0]
+    return dict(recv_xq=torch.empty(rows, ctx.fp8_row_bytes, dtype=torch.uint8, device="cuda"),
+                recv_src_rank=torch.empty(rows, dtype=torch.int32, device="cuda"),
+                recv_src_idx=torch.empty(rows, dtype=torch.int32, device="cuda"),
+                recv_topk_idx=torch.empty(rows, ctx.K, dtype=torch.int32, device="cuda"),
+                recv_topk_weights=torch.empty(rows, ctx.K, dtype=torch.float32, device="cuda"))
