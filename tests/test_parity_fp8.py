@@ -131,6 +131,7 @@ def test_quantize_every_bf16_value_for_many_scales():
     (4, 16, 4, 150, 256, 4, 0.1, 16, 4, True),       # expert-aligned blocks
     (4, 16, 4, 150, 256, 4, 0.1, 1, 5, False),       # no-wait notify, worst-case buffers
     (4, 8, 2, 0, 128, 2, 0.0, 1, 6, True),           # no tokens
+    (4, 16, 4, 40, 16384, 2, 0.0, 1, 7, True),       # largest hidden: two staged rows per CTA
 ])
 def test_quantise_and_dispatch_in_one_pass(R, E, K, T, H, C, mask_p, align, seed, wait):
     """ep_dispatch_permuted_quant gives the bytes of quantize_fp8 followed by
@@ -180,6 +181,7 @@ def test_quantise_and_dispatch_in_one_pass(R, E, K, T, H, C, mask_p, align, seed
     (16, 256, 8, 100, 7168, 8, 0.1, 2, True),
     (4, 16, 4, 150, 256, 4, 0.1, 3, False),        # no-wait notify, worst-case buffers
     (4, 8, 2, 0, 128, 2, 0.0, 4, True),            # no tokens
+    (4, 16, 4, 40, 16384, 2, 0.0, 5, True),        # largest hidden
 ])
 def test_quantise_and_scatter_in_one_pass(R, E, K, T, H, C, mask_p, seed, wait):
     """ep_dispatch_quant: the receive layout of quantize_fp8 + dispatch_fp8, and
