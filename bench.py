@@ -688,6 +688,41 @@ def main():
             two_us = statistics.median(dt_) * 1e3
             dual = {"us_two_layers": round(two_us, 2), "us_per_layer": round(two_us / 2, 2),
                     "how": "two decode microbatches (send, receive, combine each) on two streams at once"}
+            # the same two overlapped layers captured once in a CUDA graph (the
+            # streams fork from and join the capture stream) and replayed
+            try:
+                gs2 = torch.cuda.Stream()
+                gs2.wait_stream(stream)
+                torch.cuda.synchronize()
+                g2 = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g2, stream=gs2):
+                    cap = torch.cuda.current_stream()
+                    for st_, (b_, p_, o_) in zip(streams, lanes):
+                        st_.wait_stream(cap)
+                        with torch.cuda.stream(st_):
+                            b_.dispatch(d_x, d_idx_d, out=p_)
+                            b_.combine(y_ll, d_idx_d, d_w_d, p_, out=o_)
+                    for st_ in streams:
+                        cap.wait_stream(st_)
+                torch.cuda.synchronize()
+                gt2 = []
+                for i in range(args.steps + 2):
+                    flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    g2.replay()
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    if i >= 2:
+                        gt2.append(e0.elapsed_time(e1))
+                buf.check()
+                buf2.check()
+                if not torch.equal(d_out.view(torch.int16), d_out2.view(torch.int16)):
+                    raise RuntimeError("the two microbatches disagree (graph)")
+                dual["us_per_layer_cuda_graph"] = round(statistics.median(gt2) * 1e3 / 2, 2)
+                del g2
+            except Exception as exc:  # reported, not hidden
+                dual["us_per_layer_cuda_graph"] = f"capture failed: {exc}"
             del buf2, pk2, d_out2
         except Exception as exc:  # reported, not hidden
             dual = f"failed: {exc}"
