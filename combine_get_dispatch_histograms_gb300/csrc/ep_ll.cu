@@ -77,7 +77,7 @@ __host__ __device__ inline size_t ll_send_fixed_smem(int E) {
     return (off + 127) & ~size_t(127);
 }
 
-__global__ void __launch_bounds__(256) ll_send_kernel(LLSendArgs a, int stages, int64_t timeout_ns) {
+__global__ void __launch_bounds__(256, 3) ll_send_kernel(LLSendArgs a, int stages, int64_t timeout_ns) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
     int32_t* cnt = reinterpret_cast<int32_t*>(bar + kSendMaxStages);  // [E]
@@ -121,15 +121,23 @@ __global__ void __launch_bounds__(256) ll_send_kernel(LLSendArgs a, int stages, 
         const int64_t g = (int64_t)s * a.T + t;
         const int64_t my_e = nx_e;
         if (q + 1 < q1 && tid < K) nx_e = a.topk_idx[token_g(q + 1) * K + tid];
-        if (s != cur_s) {
-            // counts of this source's earlier tokens in the microbatch, per expert
-            __syncthreads();
+        // A new source: its per-expert counts restart from the source's tokens
+        // before this one (only the CTA's first token can have any; a later
+        // source change starts at token 0).  Their loads are issued now and
+        // consumed after the quantisation, which hides their latency.
+        constexpr int kScanU = 8;
+        int64_t ee[kScanU];
+        int before = 0;
+        const bool scan = s != cur_s;
+        const int64_t* first = a.topk_idx + ((int64_t)s * a.T + a.t0) * K;
+        if (scan) {
+            __syncthreads();  // thread 0 is done with the previous token's counts
             for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
-            __syncthreads();
-            const int64_t* first = a.topk_idx + ((int64_t)s * a.T + a.t0) * K;
-            for (int p = tid; p < j * K; p += blockDim.x) {
-                const int64_t e = first[p];
-                if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+            before = j * K;
+#pragma unroll
+            for (int u = 0; u < kScanU; ++u) {
+                const int p = tid + u * (int)blockDim.x;
+                ee[u] = p < before ? first[p] : -1;
             }
             cur_s = s;
         }
@@ -138,23 +146,6 @@ __global__ void __launch_bounds__(256) ll_send_kernel(LLSendArgs a, int stages, 
             if (my_e >= 0 && my_e < E) ev = (int)my_e;
             else if (my_e != -1) flag(a.status, FLAG_INVALID_TOPK);
             sh_e[tid] = ev;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            for (int k = 0; k < K; ++k) {
-                const int ev = sh_e[k];
-                int sl = -1;
-                if (ev >= 0) {
-                    sl = cnt[ev];
-                    cnt[ev] = sl + 1;
-                    if (sl >= a.cap) {
-                        flag(a.status, FLAG_CAPACITY);
-                        sl = -1;
-                    }
-                }
-                sh_slot[k] = sl;
-                a.slot_out[g * K + k] = sl;
-            }
         }
         // the staged x row of this token
         const int st = (int)(i % stages);
@@ -190,15 +181,36 @@ __global__ void __launch_bounds__(256) ll_send_kernel(LLSendArgs a, int stages, 
                 if ((gi & 7) == 0) *reinterpret_cast<float*>(msg + 16 + H + (gi >> 3) * 4) = scale;
             }
         }
+        if (scan) {
+#pragma unroll
+            for (int u = 0; u < kScanU; ++u)
+                if (ee[u] >= 0 && ee[u] < E) atomicAdd(&cnt[ee[u]], 1);
+            for (int p = tid + kScanU * (int)blockDim.x; p < before; p += blockDim.x) {
+                const int64_t e = first[p];
+                if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+            }
+        }
         if (tid == 0) *reinterpret_cast<int4*>(msg) = make_int4(t, 0, 0, 0);
         fence_proxy_async_smem();  // the message is read by the bulk copies below
         __syncthreads();
         if (tid == 0) {
+            // slots: the running per-expert counts of this source, (t, k) order
             for (int k = 0; k < K; ++k) {
-                const int sl = sh_slot[k];
-                if (sl < 0) continue;
-                bulk_s2g(a.regions + (((int64_t)sh_e[k] * R + s) * a.cap + sl) * a.msg_bytes, msg,
-                         (uint32_t)a.msg_bytes);
+                const int ev = sh_e[k];
+                int sl = -1;
+                if (ev >= 0) {
+                    sl = cnt[ev];
+                    cnt[ev] = sl + 1;
+                    if (sl >= a.cap) {
+                        flag(a.status, FLAG_CAPACITY);
+                        sl = -1;
+                    }
+                }
+                sh_slot[k] = sl;
+                a.slot_out[g * K + k] = sl;
+                if (sl >= 0)
+                    bulk_s2g(a.regions + (((int64_t)ev * R + s) * a.cap + sl) * a.msg_bytes, msg,
+                             (uint32_t)a.msg_bytes);
             }
             bulk_commit();
             // the x stage of this token is free again: stream the token `stages` ahead
