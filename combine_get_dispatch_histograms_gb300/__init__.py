@@ -214,9 +214,10 @@ class Context:
             _stream(stream)))
         h.synced = wait
         if wait:
-            h.host_num_recv_tokens = list(host_recv)
-            h.host_num_recv_per_expert = list(host_exp)
-            h.num_recv_rows, h.num_perm_rows, h.num_stage_rows = (int(v) for v in host_tot)
+            # copies of the host counts (the arrays are reused by the next notify)
+            h.host_num_recv_tokens = host_recv[:]
+            h.host_num_recv_per_expert = host_exp[:]
+            h.num_recv_rows, h.num_perm_rows, h.num_stage_rows = host_tot
         else:
             h.host_num_recv_tokens = h.host_num_recv_per_expert = None
             h.num_recv_rows, h.num_perm_rows, h.num_stage_rows = self.max_rows
