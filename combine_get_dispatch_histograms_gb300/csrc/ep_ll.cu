@@ -35,7 +35,7 @@ struct ep_ll_buffer {
     size_t bytes;
     uint8_t* regions[2];
     int32_t* counts[2];
-    uint32_t* done[2];
+    uint32_t* done[2];      // [R] completion counters of each buffer (part of the sized layout)
     uint32_t* status;
     int cur;
     int64_t wait_timeout_ns;
@@ -53,9 +53,8 @@ struct LLSendArgs {
     int32_t* slot_out;
     uint8_t* regions;
     int32_t* counts;       // [E][R] of the buffer in use
-    uint32_t* done;        // [R]
     int32_t* other_counts; // [E][R] of the other buffer
-    int R, E, K, T, H, cap, t0, n, nblk;
+    int R, E, K, T, H, cap, t0, n;
     int64_t msg_bytes;
     uint32_t* status;
 };
@@ -493,7 +492,6 @@ extern "C" ep_status ep_ll_send(ep_ll_buffer* b, const void* x, const int64_t* t
     a.slot_out = slot_out;
     a.regions = b->regions[b->cur];
     a.counts = b->counts[b->cur];
-    a.done = b->done[b->cur];
     a.other_counts = b->counts[b->cur ^ 1];
     a.R = f.num_ranks;
     a.E = f.num_experts;
@@ -503,7 +501,6 @@ extern "C" ep_status ep_ll_send(ep_ll_buffer* b, const void* x, const int64_t* t
     a.cap = b->cap;
     a.t0 = t0;
     a.n = n;
-    a.nblk = n;
     a.msg_bytes = b->msg_bytes;
     a.status = b->status;
     cudaStream_t s = as_stream(stream);
