@@ -192,3 +192,41 @@ def test_decode_ll_full():
 
 def test_skewed_ll_full_microbatches():
     _ll_full(inputs.WORKLOADS["skewed"])
+
+
+def test_prefill_full_fp8_one_pass():
+    """The one-pass FP8 dispatches at the prefill size, in the bench's launch
+    configuration: every pair row equals the two-pass form (quantise, then the
+    fused FP8 dispatch) byte for byte, and sampled rows equal the oracle's
+    quantisation of their source token."""
+    wl = inputs.WORKLOADS["prefill"]
+    R, E, K, T, H, C = wl.R, wl.E, wl.K, wl.T, wl.H, wl.num_channels
+    idx, w = inputs.make_routing(wl, 0)
+    x = inputs.make_x(wl, 0, device="cuda")
+    ctx = Context(R, E, K, T, H, num_channels=C)
+    idxd, wd = idx.cuda(), w.cuda()
+    h = ctx.notify_dispatch(idxd, ctx.get_dispatch_layout(idxd))
+    n_def = H + H // 32
+    one = ctx.dispatch_permuted_quant(x, idxd, wd, h)
+    xq = ctx.quantize_fp8(x)
+    two = ctx.dispatch_permuted_fp8(xq, idxd, wd, h)
+    ctx.check()
+    assert torch.equal(one["permuted_xq"][:, :n_def], two["permuted_xq"][:, :n_def])
+    assert torch.equal(one["perm_src_token"], two["perm_src_token"])
+    assert torch.equal(one["perm_weight"], two["perm_weight"])
+    recv = ctx.dispatch_quant(x, idxd, wd, h)
+    recv2 = ctx.dispatch_fp8(xq, idxd, wd, h)
+    ctx.check()
+    assert torch.equal(recv["recv_xq"][:, :n_def], recv2["recv_xq"][:, :n_def])
+    for k in ("recv_src_rank", "recv_src_idx", "recv_topk_idx", "recv_topk_weights"):
+        assert torch.equal(recv[k], recv2[k]), k
+    # sampled rows against the oracle's quantisation of their source token
+    rng = np.random.default_rng(3)
+    rows = rng.choice(one["permuted_xq"].shape[0], size=256, replace=False)
+    src = one["perm_src_token"].cpu().numpy()[rows]
+    xf = x.view(R * T, H)
+    got = bits(one["permuted_xq"][torch.from_numpy(rows).cuda()])
+    for i, g in enumerate(src):
+        codes, scales = orc.quantize_row(bits(xf[int(g)]))
+        eq(got[i, :H], codes, f"codes of row {rows[i]}")
+        eq(got[i, H:n_def].view(np.float32), scales, f"scales of row {rows[i]}")
