@@ -85,3 +85,70 @@ def test_ll_capacity_checks():
     with pytest.raises(EpError) as e:
         buf.check()
     assert e.value.status == "EP_ERR_CAPACITY"
+
+
+def test_one_pass_fp8_capacity_and_arguments():
+    """The one-pass FP8 dispatches: a buffer one row short is caught on the host
+    after a waiting notify and flagged on the device after a no-wait one; a
+    hidden size that is not a multiple of 128 is refused."""
+    R, E, K, T, H = 4, 16, 4, 64, 256
+    idx = inputs.random_topk(R, E, K, T, 60).cuda()
+    x = inputs.random_x(R, T, H, 60).cuda()
+    w = inputs.random_weights(R, T, K, 60).cuda()
+    ctx = Context(R, E, K, T, H, num_channels=2)
+    h = ctx.notify_dispatch(idx, ctx.get_dispatch_layout(idx))
+    rq = ctx.fp8_row_bytes
+    short = dict(permuted_xq=torch.empty(h.num_perm_rows - 1, rq, dtype=torch.uint8, device="cuda"),
+                 perm_src_token=torch.empty(h.num_perm_rows - 1, dtype=torch.int32, device="cuda"),
+                 perm_weight=torch.empty(h.num_perm_rows - 1, dtype=torch.float32, device="cuda"))
+    with pytest.raises(EpError) as e:
+        ctx.dispatch_permuted_quant(x, idx, w, h, out=short)
+    assert e.value.status == "EP_ERR_CAPACITY"
+    h2 = ctx.notify_dispatch(idx, ctx.get_dispatch_layout(idx), wait=False)
+    ctx.dispatch_permuted_quant(x, idx, w, h2, out=short)
+    with pytest.raises(EpError) as e:
+        ctx.check()
+    assert e.value.status == "EP_ERR_CAPACITY"
+    rows = h.num_recv_rows - 1
+    short_recv = dict(recv_xq=torch.empty(rows, rq, dtype=torch.uint8, device="cuda"),
+                      recv_src_rank=torch.empty(rows, dtype=torch.int32, device="cuda"),
+                      recv_src_idx=torch.empty(rows, dtype=torch.int32, device="cuda"),
+                      recv_topk_idx=torch.empty(rows, K, dtype=torch.int32, device="cuda"),
+                      recv_topk_weights=torch.empty(rows, K, dtype=torch.float32, device="cuda"))
+    ctx.dispatch_quant(x, idx, w, h2, out=short_recv)
+    with pytest.raises(EpError) as e:
+        ctx.check()
+    assert e.value.status == "EP_ERR_CAPACITY"
+    odd = Context(R, E, K, T, 136, num_channels=2)
+    x136 = inputs.random_x(R, T, 136, 60).cuda()
+    h3 = odd.notify_dispatch(idx, odd.get_dispatch_layout(idx))
+    with pytest.raises(EpError) as e:
+        odd.dispatch_quant(x136, idx, w, h3, out=short_recv)
+    assert e.value.status == "EP_ERR_INVALID_ARG"
+
+
+def test_layout_notify_argument_checks():
+    R, E, K, T = 8, 16, 2, 20
+    idx = inputs.random_topk(R, E, K, T, 61).cuda()
+    flat = Context(R, E, K, T, 64, num_channels=2)
+    lay = dict(num_tokens_per_expert=torch.empty(R, E, dtype=torch.int32, device="cuda"),
+               num_tokens_per_rank=torch.empty(R, R, dtype=torch.int32, device="cuda"),
+               is_token_in_rank=torch.empty(R, T, R, dtype=torch.uint8, device="cuda"),
+               num_tokens_per_node=torch.empty(R, 2, dtype=torch.int32, device="cuda"),
+               is_token_in_node=torch.empty(R, T, 2, dtype=torch.uint8, device="cuda"))
+    h = flat.alloc_handle()
+    with pytest.raises(EpError) as e:  # node outputs on a flat context
+        check_raw(flat, idx, lay, h)
+    assert e.value.status == "EP_ERR_INVALID_ARG"
+
+
+def check_raw(ctx, idx, lay, h):
+    """ep_layout_notify called with node outputs given (bypassing the binding's choice)."""
+    import ctypes
+    from combine_get_dispatch_histograms_gb300 import _lib
+    p = lambda t: t.data_ptr()
+    rc = ctx.lib.ep_layout_notify(ctx._ctx, p(idx), p(lay["num_tokens_per_expert"]), p(lay["num_tokens_per_rank"]),
+                                  p(lay["is_token_in_rank"]), p(lay["num_tokens_per_node"]),
+                                  p(lay["is_token_in_node"]), ctypes.byref(h.c_struct()), ctx._host_recv, None, None,
+                                  torch.cuda.current_stream().cuda_stream)
+    _lib.check("ep_layout_notify", rc)
