@@ -726,12 +726,32 @@ def main():
             del buf2, pk2, d_out2
         except Exception as exc:  # reported, not hidden
             dual = f"failed: {exc}"
+        # the pages' low-latency monitoring figures: the signal-wait distribution
+        # (count slots, one traced layer) and the buffer utilisation
+        waits = None
+        try:
+            trace = torch.zeros(dw.E, dw.R, dtype=torch.int64, device="cuda")
+            buf.trace_waits(trace)
+            flush.zero_()
+            buf.dispatch(d_x, d_idx_d, out=pk)
+            buf.combine(y_ll, d_idx_d, d_w_d, pk, out=d_out)
+            torch.cuda.synchronize()
+            buf.trace_waits(None)
+            buf.check()
+            tw = trace.flatten().double().cpu() / 1e3
+            waits = {"p50_us": round(float(tw.quantile(0.5)), 2), "p99_us": round(float(tw.quantile(0.99)), 2),
+                     "max_us": round(float(tw.max()), 2),
+                     "what": "per (expert, source): receive CTA start -> its counts read (publisher wait included)"}
+        except Exception as exc:  # reported, not hidden
+            waits = f"failed: {exc}"
+        slot_util = round(float(pk["packed_recv_count"].sum()) / (dw.E * dw.R * dw.ll_cap), 4)
         d_pairs = int((d_idx >= 0).sum())
         lbytes = ll_algo_bytes(dw.H, dw.R * dw.T, d_pairs)
         peak, _ = measured_hbm_gbs()
         ll = {"workload": "decode", "R": dw.R, "T": dw.T, "H": dw.H, "cap": dw.ll_cap,
               "us_per_layer": round(layer_us, 2), "us_per_layer_cuda_graph": graph_us,
               "dual_microbatch_overlap": dual,
+              "signal_wait": waits, "slot_utilisation": slot_util,
               "kernels": {n: {"us": round(lper[n] * 1e3, 2), "algo_bytes": lbytes[n],
                               "GBps": round(lbytes[n] / (lper[n] * 1e-3) / 1e9, 1),
                               "frac": round(lbytes[n] / (lper[n] * 1e-3) / 1e9 / peak, 3)} for n in lname},

@@ -416,6 +416,14 @@ class LLBuffer:
     def check(self, stream=None):
         check("ep_ll_check", self.lib.ep_ll_check(self._buf, _stream(stream)))
 
+    def trace_waits(self, wait_ns: Optional[torch.Tensor]):
+        """From the next receive on, write each (expert, source) signal wait (ns)
+        into wait_ns [E][R] int64 on the device; None stops the trace."""
+        if wait_ns is not None:
+            assert wait_ns.is_cuda and wait_ns.dtype == torch.int64 and wait_ns.numel() == self.E * self.R
+        self._trace = wait_ns  # kept alive while the library holds its address
+        check("ep_ll_set_wait_trace", self.lib.ep_ll_set_wait_trace(self._buf, _ptr(wait_ns)))
+
     def count_slots(self, which: int) -> int:
         return int(self.lib.ep_ll_count_slots(self._buf, which) or 0)
 

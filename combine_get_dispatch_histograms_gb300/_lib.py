@@ -66,6 +66,7 @@ SIGNATURES = {
     "ep_ll_buffer_create": (INT, [ctypes.POINTER(EpConfig), INT, ctypes.POINTER(P)]),
     "ep_ll_buffer_destroy": (None, [P]),
     "ep_ll_set_wait_timeout_us": (INT, [P, I64]),
+    "ep_ll_set_wait_trace": (INT, [P, P]),
     "ep_ll_send": (INT, [P, P, P, INT, INT, P, P]),
     "ep_ll_recv": (INT, [P, P, P, P, P, P, P]),
     "ep_ll_dispatch": (INT, [P, P, P, INT, INT, P, P, P, P, P, P, P]),

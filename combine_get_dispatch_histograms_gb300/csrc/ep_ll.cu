@@ -41,6 +41,7 @@ struct ep_ll_buffer {
     int64_t wait_timeout_ns;
     int send_ctas_per_sm;    // send kernel launch shape
     size_t send_smem_bytes;
+    int64_t* wait_trace;     // nullable device [E][R]: receive signal waits (ns)
 };
 
 namespace ep {
@@ -270,6 +271,7 @@ struct LLRecvArgs {
     int64_t msg_bytes;
     int64_t timeout_ns;
     uint32_t* status;
+    int64_t* wait_trace;  // nullable [E][R]: ns from the CTA's start until its counts were read
 };
 
 // Bounded poll of one count slot: the sentinel -1 means "not written yet".
@@ -298,6 +300,7 @@ __global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(LLRecvArgs a) {
     __shared__ int sh_begin, sh_count;
     const int s = blockIdx.x, e = blockIdx.y;
     const int z = blockIdx.z, Z = gridDim.z;  // this CTA's share of the region's messages
+    const uint64_t t_start = a.wait_trace ? globaltimer_ns() : 0;
     // launched as a programmatic dependent of the count publisher: start once
     // its grid (and every write before it) is complete
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -322,6 +325,8 @@ __global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(LLRecvArgs a) {
             }
             sh_begin = before;
             sh_count = mine;
+            // the signal wait: from this CTA's start until its counts were read
+            if (a.wait_trace && z == 0) a.wait_trace[(int64_t)e * R + s] = (int64_t)(globaltimer_ns() - t_start);
         }
     }
     __syncthreads();
@@ -461,6 +466,12 @@ extern "C" ep_status ep_ll_set_wait_timeout_us(ep_ll_buffer* b, int64_t us) {
     return EP_OK;
 }
 
+extern "C" ep_status ep_ll_set_wait_trace(ep_ll_buffer* b, int64_t* wait_ns) {
+    if (!b) return set_error(EP_ERR_INVALID_ARG, "buffer is NULL");
+    b->wait_trace = wait_ns;
+    return EP_OK;
+}
+
 extern "C" ep_status ep_ll_check(ep_ll_buffer* b, void* stream) {
     if (!b) return set_error(EP_ERR_INVALID_ARG, "buffer is NULL");
     uint32_t flags = 0;
@@ -560,6 +571,7 @@ extern "C" ep_status ep_ll_recv(ep_ll_buffer* b, uint8_t* packed_x, float* packe
     a.msg_bytes = b->msg_bytes;
     a.timeout_ns = b->wait_timeout_ns;
     a.status = b->status;
+    a.wait_trace = b->wait_trace;
     cudaLaunchConfig_t lc = {};
     // split a region's messages over Z CTAs when a full region is large (about
     // 512 KB per CTA), so hot experts do not serialise on one CTA

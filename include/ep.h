@@ -388,6 +388,13 @@ void ep_ll_buffer_destroy(ep_ll_buffer* buf);
 /* Limit of the receiver's count-slot waits, microseconds (default 100 000). */
 ep_status ep_ll_set_wait_timeout_us(ep_ll_buffer* buf, int64_t us);
 
+/* Signal-wait trace ([P1] 工程实践：模式选择与监控要点, the low-latency mode's
+ * count-slot wait distribution): with wait_ns a caller-owned device array
+ * [E][R] int64, every later ep_ll_recv writes, per (expert e, source s), the
+ * nanoseconds from its receive CTA's start until that CTA had read the counts
+ * it needs (the wait for the publisher included).  NULL stops the trace. */
+ep_status ep_ll_set_wait_trace(ep_ll_buffer* buf, int64_t* wait_ns);
+
 /* Sends the microbatch of tokens [t0, t0+n) of every source rank (n <= cap):
  * flips to the other ping-pong buffer, quantises each token once to e4m3 with
  * per-128-channel fp32 scales (scale = amax / 448, code = RNE-satfinite(x /

@@ -152,3 +152,26 @@ def check_raw(ctx, idx, lay, h):
                                   p(lay["is_token_in_node"]), ctypes.byref(h.c_struct()), ctx._host_recv, None, None,
                                   torch.cuda.current_stream().cuda_stream)
     _lib.check("ep_layout_notify", rc)
+
+
+def test_ll_signal_wait_trace():
+    """The receive's signal-wait trace: about the time limit when nothing was
+    sent, small waits once the counts are published."""
+    R, E, K, T, H, cap = 4, 8, 2, 8, 128, 8
+    buf = LLBuffer(R, E, K, T, H, cap)
+    trace = torch.full((E, R), -1, dtype=torch.int64, device="cuda")
+    buf.trace_waits(trace)
+    buf.set_wait_timeout_us(20_000)
+    pk = buf.alloc_packed()
+    buf.recv(pk)  # a fresh buffer: its count slots still hold the sentinel
+    with pytest.raises(EpError):
+        buf.check()
+    assert (trace.cpu() >= 20_000_000).all()             # each receive waited out its 20 ms
+    trace.fill_(-1)
+    idx = inputs.random_topk(R, E, K, T, 0).cuda()
+    x = inputs.random_x(R, T, H, 0).cuda()
+    buf.dispatch(x, idx)
+    buf.check()
+    t = trace.cpu()
+    assert (t >= 0).all() and (t < 20_000_000).all()      # every (expert, source) written, under the limit
+    buf.trace_waits(None)
