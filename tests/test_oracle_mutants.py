@@ -57,6 +57,10 @@ MUTANTS = [
      "volatile float a = final_sum + partial;\n                        final_sum = a;"),
     ("home rank by node of the source",
      "if (s % G != h % G) continue;", "if (s / G != h % G) continue;"),
+    ("expert blocks not rounded to the alignment",
+     "acc += round_up(n, align);", "acc += n;"),
+    ("aligned permute places a block at its unpadded start",
+     "row += padded;\n        i = j;", "row += cnt;\n        i = j;"),
 ]
 
 
