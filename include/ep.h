@@ -24,9 +24,9 @@
  *     ([..][H]) and fp8 ([..][H]) must be 16-byte aligned.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  Every call is asynchronous on that stream, except
- *     ep_notify_dispatch in its waiting form (it waits for the receive
- *     counts, the one host synchronisation of the normal path) and the
- *     *_check calls.
+ *     ep_notify_dispatch and ep_layout_notify in their waiting forms (they
+ *     wait for the receive counts, the one host synchronisation of the normal
+ *     path) and the *_check calls.
  *   - bf16 values are passed as void* (2 bytes each); topk_idx is int64 with -1
  *     meaning "masked" (the entry is ignored everywhere); topk_weights fp32.
  *   - Return EP_OK or a negative ep_status; the message of the last failure on
@@ -34,7 +34,7 @@
  *     host before any launch.  Errors found on the device (a topk_idx value
  *     outside [-1, E), a full low-latency region, a wait that ran out) are
  *     recorded in a device status word and reported by ep_ctx_check /
- *     ep_ll_check (ep_notify_dispatch reports them too, since it synchronises).
+ *     ep_ll_check (the waiting notify reports them too, since it synchronises).
  */
 #ifndef EP_GB300_H
 #define EP_GB300_H
