@@ -14,29 +14,52 @@ namespace ep {
 
 __host__ __device__ inline int64_t fp8_row_bytes(int H) { return ((int64_t)H + H / 32 + 15) / 16 * 16; }
 
-// grid-stride over tokens; one thread per 16 channels, 8 lanes per 128-channel block
+// Items are (token, 16-channel group) pairs in row-major order; thread i of
+// the grid takes items i, i + S, ... (S = grid threads), kU of them per round
+// with all their loads issued before the first is quantised, so that each
+// warp keeps kU KB of x in flight.  S and each block's first item are
+// multiples of 8, and so is the number of groups per row, so an aligned group
+// of 8 lanes always holds one whole 128-channel block (or none).
+constexpr int kQuantU = 2;
+
+template <typename Idx>
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ xq,
                                                             int64_t tokens, int H) {
     const int64_t row_q = fp8_row_bytes(H);
-    const int ngroups = H / 16;
-    for (int64_t g = blockIdx.x; g < tokens; g += gridDim.x) {
-        const uint16_t* xr = x + g * H;
-        uint8_t* q = xq + g * row_q;
-        for (int gi0 = 0; gi0 < ngroups; gi0 += blockDim.x) {
-            const int gi = gi0 + threadIdx.x;
-            const bool act = gi < ngroups;
+    const Idx ng = (Idx)(H / 16);
+    const Idx total = (Idx)tokens * ng;
+    const Idx S = (Idx)gridDim.x * blockDim.x;
+    for (Idx r0 = (Idx)blockIdx.x * blockDim.x; r0 < total; r0 += S * kQuantU) {
+        int4 p[kQuantU][2];
+        Idx g[kQuantU], gi[kQuantU];
+        bool act[kQuantU];
+#pragma unroll
+        for (int u = 0; u < kQuantU; ++u) {
+            const Idx i = r0 + (Idx)u * S + threadIdx.x;
+            act[u] = i < total;
+            g[u] = i / ng;
+            gi[u] = i - g[u] * ng;
+            if (act[u]) {
+                const uint16_t* src = x + (int64_t)g[u] * H + (int64_t)gi[u] * 16;
+                p[u][0] = ld_nc_na_v4(src);
+                p[u][1] = ld_nc_na_v4(src + 8);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kQuantU; ++u) {
             float v[16];
-            if (act) {
-                bf16x16_to_f32(ld_nc_na_v4(xr + gi * 16), ld_nc_na_v4(xr + gi * 16 + 8), v);
+            if (act[u]) {
+                bf16x16_to_f32(p[u][0], p[u][1], v);
             } else {
 #pragma unroll
-                for (int u = 0; u < 16; ++u) v[u] = 0.0f;
+                for (int k = 0; k < 16; ++k) v[k] = 0.0f;
             }
             float scale;
             const int4 codes = quantize16(v, &scale);
-            if (act) {
-                st_na_v4(q + (size_t)gi * 16, codes);
-                if ((gi & 7) == 0) reinterpret_cast<float*>(q + H)[gi >> 3] = scale;
+            if (act[u]) {
+                uint8_t* q = xq + (int64_t)g[u] * row_q;
+                st_na_v4(q + (int64_t)gi[u] * 16, codes);
+                if ((gi[u] & 7) == 0) reinterpret_cast<float*>(q + H)[gi[u] >> 3] = scale;
             }
         }
     }
@@ -244,12 +267,21 @@ extern "C" ep_status ep_quantize_fp8(ep_ctx* c, const void* x, uint8_t* xq, void
     const int64_t tokens = (int64_t)c->cfg.num_ranks * c->cfg.num_tokens;
     if (tokens == 0) return EP_OK;
     if (!x || !xq || !aligned16(x) || !aligned16(xq)) return set_error(EP_ERR_INVALID_ARG, "x and xq must be 16-byte aligned");
-    int64_t grid = (int64_t)c->num_sms * 8;
-    if (grid > tokens) grid = tokens;
-    int threads = ((c->cfg.hidden / 16 + 31) / 32) * 32;
-    if (threads > 256) threads = 256;
-    quantize_rows_kernel<<<(int)grid, threads, 0, as_stream(stream)>>>(static_cast<const uint16_t*>(x), xq, tokens,
-                                                                       c->cfg.hidden);
+    // one wave of resident CTAs
+    const int64_t total = tokens * (c->cfg.hidden / 16);
+    const bool narrow = total <= (int64_t)UINT32_MAX - 2 * kQuantU * 256 * (int64_t)c->num_sms * 8;
+    int per_sm = 0;
+    EP_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, narrow ? quantize_rows_kernel<uint32_t> : quantize_rows_kernel<uint64_t>, 256, 0));
+    if (per_sm < 1) per_sm = 1;
+    if (per_sm > 8) per_sm = 8;
+    int64_t grid = (int64_t)c->num_sms * per_sm;
+    if (grid > (total + 255) / 256) grid = (total + 255) / 256;
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    if (narrow)
+        quantize_rows_kernel<uint32_t><<<(int)grid, 256, 0, as_stream(stream)>>>(xb, xq, tokens, c->cfg.hidden);
+    else
+        quantize_rows_kernel<uint64_t><<<(int)grid, 256, 0, as_stream(stream)>>>(xb, xq, tokens, c->cfg.hidden);
     EP_CHECK_LAUNCH("quantize_rows_kernel");
     c->last_launches = 1;
     return EP_OK;

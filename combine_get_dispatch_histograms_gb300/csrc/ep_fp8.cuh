@@ -1,7 +1,7 @@
 // ep_fp8.cuh -- the e4m3 codec shared by the low-latency send and the FP8
 // normal-mode rows: per 128 channels, scale = amax / 448 (IEEE fp32 division),
-// code = cvt.rn.satfinite.e4m3 of x / scale (IEEE division); a zero scale
-// keeps only the sign of x.
+// code = cvt.rn.satfinite.e4m3 of x / scale (the IEEE fp32 quotient); a zero
+// scale keeps only the sign of x.
 #pragma once
 #include <cuda_fp8.h>
 
@@ -25,6 +25,27 @@ __device__ __forceinline__ void bf16x16_to_f32(const int4& p0, const int4& p1, f
     }
 }
 
+// x / scale as the IEEE (round-to-nearest) fp32 quotient, from y = RN(1/scale)
+// computed once per block: q0 = RN(x*y), the exact residual r = q0*scale - x
+// by one fma, then q = RN(q0 - r*y).  This is Markstein's correction step
+// (P. Markstein, IBM J. Res. Dev. 34(1), 1990): with y correctly rounded and
+// q0 within an ulp of the quotient, q is the correctly rounded quotient as
+// long as nothing underflows.  Over every pair of a bf16 x and a bf16 block
+// maximum with |x| <= amax and scale >= 2^-100, the e4m3 code of q equals the
+// code of the IEEE quotient (checked exhaustively); q can differ from it only
+// below 2^-10, where both codes are +-0 with x's sign.  The residual's sign
+// convention keeps that sign for x = -0.
+__device__ __forceinline__ float div_by_scale(float x, float scale, float y) {
+    const float q0 = __fmul_rn(x, y);
+    const float r = __fmaf_rn(q0, scale, -x);
+    return __fmaf_rn(-r, y, q0);
+}
+
+// Scales below this (block maxima under ~3.5e-28) and non-finite ones take
+// the IEEE division instruction sequence per element instead.
+constexpr float kRcpScaleMin = 0x1p-100f;
+constexpr float kRcpScaleMax = 3.0e38f;
+
 // Quantises the 16 channels a lane holds; the 8 lanes of an aligned lane group
 // hold one 128-channel block and share its scale.  Every lane of the warp must
 // call it (shuffles); lanes without data pass zeros.
@@ -43,6 +64,14 @@ __device__ __forceinline__ int4 quantize16(const float* v, float* scale_out) {
 #pragma unroll
             for (int b = 0; b < 4; ++b) c |= ((__float_as_uint(v[4 * u + b]) >> 31) ? 0x80u : 0u) << (8 * b);
             w4[u] = c;
+        }
+    } else if (scale >= kRcpScaleMin && scale <= kRcpScaleMax) {
+        const float y = __frcp_rn(scale);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t lo = e4m3x2(div_by_scale(v[4 * u], scale, y), div_by_scale(v[4 * u + 1], scale, y));
+            const uint32_t hi = e4m3x2(div_by_scale(v[4 * u + 2], scale, y), div_by_scale(v[4 * u + 3], scale, y));
+            w4[u] = (lo & 0xffffu) | (hi << 16);
         }
     } else {
 #pragma unroll

@@ -89,8 +89,10 @@ def test_quantize_every_bf16_value_for_many_scales():
                0x3f80, 0x4040, 0x4030, 0x3e99, 0x3a83, 0x3c8c, 0x40a0, 0x40e0, 0x449a,
                0x7f7f,  # largest finite bf16
                0x0080,  # smallest normal bf16
-               0x0001, 0x0040]  # subnormal block maxima
-    amaxes = special + [int(b) for b in rng.integers(0x2000, 0x5000, size=10)]
+               0x0001, 0x0040,  # subnormal block maxima
+               0x11DF, 0x11E0, 0x11E1]  # scales on both sides of 2^-100 (the division fallback)
+    amaxes = (special + [int(b) for b in rng.integers(0x2000, 0x5000, size=10)]
+              + [int(b) for b in rng.integers(0x0001, 0x7F80, size=16)])
     blocks = []
     for a in amaxes:
         vals = _bf16_values_up_to(a)
