@@ -40,6 +40,25 @@ TRAFFIC = {
 }
 
 
+NOMINAL_HBM_GBS = 8000.0  # the metric's "% of ~8 TB/s"
+
+
+def add_nominal_pct(obj):
+    """Beside every effective GB/s figure, its percentage of the nominal ~8 TB/s
+    the metric names (the `frac` keys stay fractions of the measured peak)."""
+    if isinstance(obj, dict):
+        for k in list(obj):
+            v = obj[k]
+            if k in ("GBps", "effective_GBps") and isinstance(v, (int, float)):
+                obj[k.replace("GBps", "pct_of_8TBps")] = round(100.0 * v / NOMINAL_HBM_GBS, 1)
+            else:
+                add_nominal_pct(v)
+    elif isinstance(obj, list):
+        for v in obj:
+            add_nominal_pct(v)
+    return obj
+
+
 def measured_hbm_gbs():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -971,7 +990,7 @@ def main():
         "graph": nw_graph,
         "fp8_rows": fp8,
     }
-    print(json.dumps(line), flush=True)
+    print(json.dumps(add_nominal_pct(line)), flush=True)
     epdist.shutdown()
     return 0
 
