@@ -29,6 +29,24 @@ if ROOT not in sys.path:
 
 METRIC = "dispatch+combine tokens/s and effective HBM GB/s (% of ~8 TB/s); LL µs/layer"
 L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
+L2_DESC = ("flushed before each timed region, not timed: a 512 MiB write, then a 512 MiB read of a second "
+           "buffer, so that L2 holds none of the inputs and none of the flush's own dirty lines")
+
+
+class L2Flush:
+    """Cold-L2 reset between timed iterations.  Writing a buffer larger than L2
+    evicts the inputs but leaves L2 full of the buffer's dirty lines, whose
+    write-back would then be charged to the first timed kernel (~7 us of the
+    decode send); reading a second such buffer afterwards writes them back
+    before the timed region starts."""
+
+    def __init__(self, torch):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.max()
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) per launch of the dominant kernel, from the ncu
@@ -244,10 +262,12 @@ def run_ll_only(args):
     y = torch.zeros(pk["packed_x"].shape, dtype=torch.bfloat16, device="cuda")
     out = torch.empty(dw.R, dw.T, dw.H, dtype=torch.bfloat16, device="cuda")
     st = torch.cuda.current_stream()
+    flush = L2Flush(torch)
     times = []
     mbs = [(t0, min(dw.ll_cap, dw.T - t0)) for t0 in range(0, dw.T, dw.ll_cap)]  # microbatches of <= cap tokens
     for i in range(args.warmup + args.steps):
         for t0, n in mbs:
+            flush()
             e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
             e[0].record(st)
             buf.send(x, idxd, t0, n, out=pk)
@@ -346,7 +366,7 @@ def main():
     idx_d, w_d = topk_idx.cuda(), topk_w.cuda()
     ctx = Context(R, E, K, T, H, num_channels=C, num_nodes=w.num_nodes)
     stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush(torch)
 
     # sizes from one notify, then buffers allocated once
     lay = ctx.get_dispatch_layout(idx_d, nodes=hier)
@@ -387,7 +407,7 @@ def main():
         mark(5)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     ctx.check()
     torch.cuda.synchronize()
@@ -400,7 +420,7 @@ def main():
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush.zero_()  # L2 flush between steps, outside the step's events
+        flush()  # L2 flush between steps, outside the step's events
         step(evs[i])
     torch.cuda.synchronize()
     barrier()
@@ -438,11 +458,11 @@ def main():
             mark(4)
 
         for _ in range(args.warmup):
-            flush.zero_()
+            flush()
             fstep()
         fev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
         for i in range(args.steps):
-            flush.zero_()
+            flush()
             fstep(fev[i])
         torch.cuda.synchronize()
         ctx.check()
@@ -504,11 +524,11 @@ def main():
             with torch.cuda.graph(cg):
                 fn()
             for _ in range(args.warmup):
-                flush.zero_()
+                flush()
                 cg.replay()
             gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
             for i in range(args.steps):
-                flush.zero_()
+                flush()
                 gev[i][0].record(stream)
                 cg.replay()
                 gev[i][1].record(stream)
@@ -534,12 +554,12 @@ def main():
                   perm_src_token=torch.empty(pairs, dtype=torch.int32, device="cuda"),
                   perm_weight=torch.empty(pairs, dtype=torch.float32, device="cuda"))
         for _ in range(args.warmup):
-            flush.zero_()
+            flush()
             ctx.quantize_fp8(x, out=xq)
             ctx.dispatch_permuted_fp8(xq, idx_d, w_d, handle, out=fq)
         qt, dt = [], []
         for i in range(args.steps):
-            flush.zero_()
+            flush()
             e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
             e[0].record(stream)
             ctx.quantize_fp8(x, out=xq)
@@ -556,7 +576,7 @@ def main():
         # quantisation fused into the dispatch: one pass from the bf16 tokens
         ot = []
         for i in range(args.warmup + args.steps):
-            flush.zero_()
+            flush()
             e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
             e[0].record(stream)
             ctx.dispatch_permuted_quant(x, idx_d, w_d, handle, out=fq)
@@ -573,7 +593,7 @@ def main():
                        recv_topk_weights=torch.empty(copies, K, dtype=torch.float32, device="cuda"))
         st_ = []
         for i in range(args.warmup + args.steps):
-            flush.zero_()
+            flush()
             e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
             e[0].record(stream)
             ctx.dispatch_quant(x, idx_d, w_d, handle, out=rq_recv)
@@ -619,13 +639,13 @@ def main():
         del codes
         d_out = torch.empty(dw.R, dw.T, dw.H, dtype=torch.bfloat16, device="cuda")
         for _ in range(args.warmup):
-            flush.zero_()
+            flush()
             buf.dispatch(d_x, d_idx_d, out=pk)
             buf.combine(y_ll, d_idx_d, d_w_d, pk, out=d_out)
         buf.check()
         lev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
         for i in range(args.steps):
-            flush.zero_()
+            flush()
             lev[i][0].record(stream)
             buf.send(d_x, d_idx_d, out=pk)
             lev[i][1].record(stream)
@@ -655,7 +675,7 @@ def main():
             torch.cuda.synchronize()
             gt = []
             for i in range(args.steps + 2):
-                flush.zero_()
+                flush()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 graph.replay()
@@ -689,11 +709,11 @@ def main():
                     stream.wait_stream(st_)
 
             for _ in range(args.warmup):
-                flush.zero_()
+                flush()
                 dual_layer()
             dt_ = []
             for i in range(args.steps):
-                flush.zero_()
+                flush()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 dual_layer()
@@ -726,7 +746,7 @@ def main():
                 torch.cuda.synchronize()
                 gt2 = []
                 for i in range(args.steps + 2):
-                    flush.zero_()
+                    flush()
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     e0.record(stream)
                     g2.replay()
@@ -751,7 +771,7 @@ def main():
         try:
             trace = torch.zeros(dw.E, dw.R, dtype=torch.int64, device="cuda")
             buf.trace_waits(trace)
-            flush.zero_()
+            flush()
             buf.dispatch(d_x, d_idx_d, out=pk)
             buf.combine(y_ll, d_idx_d, d_w_d, pk, out=d_out)
             torch.cuda.synchronize()
@@ -774,7 +794,7 @@ def main():
               "kernels": {n: {"us": round(lper[n] * 1e3, 2), "algo_bytes": lbytes[n],
                               "GBps": round(lbytes[n] / (lper[n] * 1e-3) / 1e9, 1),
                               "frac": round(lbytes[n] / (lper[n] * 1e-3) / 1e9 / peak, 3)} for n in lname},
-              "l2": "flushed before each layer (512 MiB write), flush not timed"}
+              "l2": L2_DESC}
         del y_ll, pk, buf
 
     clocks = sampler.stop()
@@ -897,7 +917,7 @@ def main():
         def timed(step_fn):
             run(max(2, args.warmup), step_fn)
             torch.cuda.synchronize()
-            flush.zero_()
+            flush()
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -975,7 +995,7 @@ def main():
         "config": {"workload": w.name, "R": R, "E": E, "K": K, "T": T, "H": H, "num_channels": C,
                    "num_nodes": w.num_nodes, "router": w.router, "tokens_per_step_per_gpu": tokens,
                    "copies": copies, "pairs": pairs,
-                   "l2": "flushed between steps (512 MiB write, not timed); every step's inputs exceed L2",
+                   "l2": L2_DESC + "; every step's inputs exceed L2 anyway",
                    "timing": "CUDA events on the launching stream, per step, mean over steps, max over ranks"},
         "effective_GBps": round(sum(ab.values()) / (sum(med[n] for n in ab) * 1e-3) / 1e9, 1),
         "kernels": kernels,
