@@ -219,11 +219,17 @@ __device__ void notify_global_scan(const NotifyArgs& a, int32_t* sh /* >= 2E + 3
     // a thread are independent, so each phase costs one memory round trip.
     for (int d = threadIdx.x; d < R; d += blockDim.x) {
         int32_t acc = 0;
-        for (int s = 0; s < R; ++s) {
-            const int32_t c = a.ntpr[s * R + d];
-            a.h.recv_count[d * R + s] = c;
-            a.h.recv_offsets[d * R + s] = acc;
-            acc += c;
+        for (int s0 = 0; s0 < R; s0 += 16) {  // loads first: the stores may alias them
+            int32_t c[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) c[u] = s0 + u < R ? a.ntpr[(s0 + u) * R + d] : 0;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                if (s0 + u >= R) break;
+                a.h.recv_count[d * R + s0 + u] = c[u];
+                a.h.recv_offsets[d * R + s0 + u] = acc;
+                acc += c[u];
+            }
         }
         a.h.num_recv_tokens[d] = acc;
         a.host[d] = acc;
@@ -231,6 +237,7 @@ __device__ void notify_global_scan(const NotifyArgs& a, int32_t* sh /* >= 2E + 3
     }
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int32_t acc = 0;
+#pragma unroll 16
         for (int s = 0; s < R; ++s) acc += a.ntpe[(int64_t)s * E + e];
         tot[e] = acc;
         a.h.num_recv_per_expert[e] = acc;  // [d][l] flattened == e
@@ -272,9 +279,16 @@ __device__ void notify_global_scan(const NotifyArgs& a, int32_t* sh /* >= 2E + 3
         const int32_t o = off[e];
         a.h.expert_offsets[e] = o - off[(e / L) * L];
         int32_t acc = o;
-        for (int s = 0; s < R; ++s) {
-            a.ebase[(int64_t)s * E + e] = acc;
-            acc += a.ntpe[(int64_t)s * E + e];
+        for (int s0 = 0; s0 < R; s0 += 16) {  // loads first: the stores may alias them
+            int32_t c[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) c[u] = s0 + u < R ? a.ntpe[(int64_t)(s0 + u) * E + e] : 0;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                if (s0 + u >= R) break;
+                a.ebase[(int64_t)(s0 + u) * E + e] = acc;
+                acc += c[u];
+            }
         }
     }
     // (e) hierarchical staging bases: home rank h of node n = h / G receives
