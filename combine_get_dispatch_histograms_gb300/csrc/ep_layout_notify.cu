@@ -688,6 +688,12 @@ extern "C" ep_status ep_ctx_set_wait_timeout_us(ep_ctx* c, int64_t us) {
 
 extern "C" ep_status ep_ctx_set_expert_alignment(ep_ctx* c, int32_t alignment) {
     if (!c || alignment < 1 || alignment > (1 << 16)) return set_error(EP_ERR_INVALID_ARG, "bad context or alignment");
+    // permuted rows (int32 positions) are at most R*T*K plus E*(alignment-1) of padding
+    const ep_config& f = c->cfg;
+    const int64_t worst = (int64_t)f.num_ranks * f.num_tokens * f.num_topk + (int64_t)f.num_experts * (alignment - 1);
+    if (worst >= (1ll << 31))
+        return set_error(EP_ERR_INVALID_ARG, "alignment %d: R*T*K + E*(alignment-1) = %lld must stay below 2^31",
+                         alignment, (long long)worst);
     c->expert_alignment = alignment;
     return EP_OK;
 }

@@ -93,7 +93,8 @@ ep_status ep_ctx_check(ep_ctx* ctx, void* stream);
  * (copy-pipeline barriers).  Default 2 000 000. */
 ep_status ep_ctx_set_wait_timeout_us(ep_ctx* ctx, int64_t us);
 
-/* Expert alignment of the permuted layout (default 1 = none; 1..65536).
+/* Expert alignment of the permuted layout (default 1 = none; 1..65536, and
+ * R*T*K + E*(alignment-1) below 2^31, else EP_ERR_INVALID_ARG).
  * The pages fix none; it serves a grouped GEMM that wants every expert's
  * block to start on a tile boundary.  From the next ep_notify_dispatch on,
  * each (rank d, local expert l) block of the permuted layout takes

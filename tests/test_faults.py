@@ -175,3 +175,24 @@ def test_ll_signal_wait_trace():
     t = trace.cpu()
     assert (t >= 0).all() and (t < 20_000_000).all()      # every (expert, source) written, under the limit
     buf.trace_waits(None)
+
+
+def test_expert_alignment_limits():
+    """Alignments outside 1..65536, or whose padding would push the permuted
+    row count past the int32 positions, are rejected on the host and leave
+    the alignment in force unchanged."""
+    ctx = Context(4, 8, 2, 16, 64, num_channels=1)
+    for bad in (0, -3, 65537):
+        with pytest.raises(EpError) as e:
+            ctx.set_expert_alignment(bad)
+        assert e.value.status == "EP_ERR_INVALID_ARG"
+    assert ctx.expert_alignment == 1
+    # R*T*K = 32 * 1 970 000 * 32 ~ 2.017e9: E*(alignment-1) = 2048*1023 still fits
+    # below 2^31, 2048*65535 does not (the context holds a ~4 GB workspace)
+    big = Context(32, 2048, 32, 1_970_000, 128, num_channels=1)
+    big.set_expert_alignment(1024)
+    with pytest.raises(EpError) as e:
+        big.set_expert_alignment(65536)
+    assert e.value.status == "EP_ERR_INVALID_ARG"
+    assert big.expert_alignment == 1024
+    big.close()
