@@ -16,10 +16,11 @@
 // kernel quantises each token once (per-128-channel amax, IEEE division,
 // cvt.rn.satfinite.e4m3x2) and stores the message to its K regions; slots are
 // the deterministic (t, k)-order rank of the entry among the source's entries
-// for the same expert (no atomic slot claims); the last CTA of a source
-// (completion counter) publishes all counts of that source with st.release
-// after the data, 0 included.  The receive kernel polls each count with
-// ld.acquire under a time limit and packs the messages.
+// for the same expert (no atomic slot claims); a publisher kernel, launched as
+// a programmatic dependent of the send, stores every count of every source
+// with st.release once the send grid has completed, 0 included.  The receive
+// kernel polls each count with ld.acquire under a time limit and packs the
+// messages.
 #include <cuda_fp8.h>
 #include <cstdlib>
 
@@ -35,7 +36,6 @@ struct ep_ll_buffer {
     size_t bytes;
     uint8_t* regions[2];
     int32_t* counts[2];
-    uint32_t* done[2];      // [R] completion counters of each buffer (part of the sized layout)
     uint32_t* status;
     int cur;
     int64_t wait_timeout_ns;
@@ -385,8 +385,7 @@ extern "C" int64_t ep_ll_message_bytes(int hidden) {
 
 static int64_t ll_one_buffer_bytes(int cap, int H, int R, int E) {
     const int64_t counts = ((int64_t)E * R * 4 + 15) / 16 * 16;
-    const int64_t done = ((int64_t)R * 4 + 15) / 16 * 16;
-    int64_t one = (int64_t)E * R * cap * ep_ll_message_bytes(H) + counts + done;
+    int64_t one = (int64_t)E * R * cap * ep_ll_message_bytes(H) + counts;
     return (one + 127) / 128 * 128;
 }
 
@@ -431,19 +430,14 @@ extern "C" ep_status ep_ll_buffer_create(const ep_config* cfg, int cap, ep_ll_bu
     }
     uint8_t* base = static_cast<uint8_t*>(b->mem);
     const int64_t reg = (int64_t)E * R * cap * b->msg_bytes;
-    const int64_t counts = ((int64_t)E * R * 4 + 15) / 16 * 16;
     for (int i = 0; i < 2; ++i) {
         uint8_t* p = base + i * one;
         b->regions[i] = p;
         b->counts[i] = reinterpret_cast<int32_t*>(p + reg);
-        b->done[i] = reinterpret_cast<uint32_t*>(p + reg + counts);
     }
     b->status = reinterpret_cast<uint32_t*>(base + 2 * one);
-    // counts start at the empty sentinel; completion counters and status at 0
-    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
-        e = cudaMemset(b->counts[i], 0xff, (size_t)E * R * 4);
-        if (e == cudaSuccess) e = cudaMemset(b->done[i], 0, (size_t)R * 4);
-    }
+    // counts start at the empty sentinel, the status word at 0
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaMemset(b->counts[i], 0xff, (size_t)E * R * 4);
     if (e == cudaSuccess) e = cudaMemset(b->status, 0, 4);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {

@@ -374,8 +374,8 @@ typedef struct ep_ll_buffer ep_ll_buffer;
 int64_t ep_ll_message_bytes(int hidden);
 
 /* Bytes the two ping-pong buffers take ([P3] 2.2 get_low_latency_rdma_size_hint):
- * per buffer E*R*cap messages, E*R int32 count slots and R int32 completion
- * counters (each padded to 16 bytes), rounded up to a multiple of 128.
+ * per buffer E*R*cap messages and E*R int32 count slots (padded to 16
+ * bytes), rounded up to a multiple of 128.
  * Worst case by construction: every (expert, source) region holds `cap`. */
 int64_t ep_ll_size_hint(int num_max_dispatch_tokens_per_rank, int hidden, int num_ranks,
                         int num_experts);

@@ -432,11 +432,9 @@ int64_t orc_ll_message_bytes(int H) {
 
 int64_t orc_ll_size_hint(int cap, int H, int R, int E) {
     /* two ping-pong buffers, each: E*R*cap messages + E*R int32 count slots
-     * (padded to 16 bytes) + R int32 completion counters (padded to 16),
-     * rounded up to a multiple of 128 bytes */
+     * (padded to 16 bytes), rounded up to a multiple of 128 bytes */
     int64_t counts = ((int64_t)E * R * 4 + 15) / 16 * 16;
-    int64_t done = ((int64_t)R * 4 + 15) / 16 * 16;
-    int64_t one = (int64_t)E * R * cap * orc_ll_message_bytes(H) + counts + done;
+    int64_t one = (int64_t)E * R * cap * orc_ll_message_bytes(H) + counts;
     one = (one + 127) / 128 * 128;
     return 2 * one;
 }

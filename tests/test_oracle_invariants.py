@@ -176,7 +176,7 @@ def test_size_hint(orc):
         msg = orc.ll_message_bytes(H)
         assert msg >= 16 + H + H // 128 * 4 and msg % 16 == 0
         need = 2 * (E * R * cap * msg + E * R * 4)
-        assert hint >= need and hint % 128 == 0 and hint - need < 2 * (128 + 32 + 4 * R)
+        assert hint >= need and hint % 128 == 0 and hint - need < 2 * (128 + 16)
 
 
 def test_invalid_topk_reported(orc):
