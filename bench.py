@@ -657,7 +657,20 @@ def main():
         buf.check()
         lname = ["ll_send", "ll_recv", "ll_combine"]
         lper = {n: statistics.median(e[j].elapsed_time(e[j + 1]) for e in lev) for j, n in enumerate(lname)}
-        layer_us = statistics.median(e[0].elapsed_time(e[3]) for e in lev) * 1e3
+        layer_instrumented_us = statistics.median(e[0].elapsed_time(e[3]) for e in lev) * 1e3
+        # the layer alone, events only at its ends: the per-kernel events above
+        # sit between the programmatic-dependent launches and serialise them
+        lay_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush()
+            lay_ev[i][0].record(stream)
+            buf.send(d_x, d_idx_d, out=pk)
+            buf.recv(pk)
+            buf.combine(y_ll, d_idx_d, d_w_d, pk, out=d_out)
+            lay_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        buf.check()
+        layer_us = statistics.median(e[0].elapsed_time(e[1]) for e in lay_ev) * 1e3
         # the same layer captured once in a CUDA graph and replayed (static shapes,
         # no host sync, no allocation inside the layer)
         graph_us = None
@@ -788,7 +801,9 @@ def main():
         lbytes = ll_algo_bytes(dw.H, dw.R * dw.T, d_pairs)
         peak, _ = measured_hbm_gbs()
         ll = {"workload": "decode", "R": dw.R, "T": dw.T, "H": dw.H, "cap": dw.ll_cap,
-              "us_per_layer": round(layer_us, 2), "us_per_layer_cuda_graph": graph_us,
+              "us_per_layer": round(layer_us, 2),
+              "us_per_layer_with_kernel_events": round(layer_instrumented_us, 2),
+              "us_per_layer_cuda_graph": graph_us,
               "dual_microbatch_overlap": dual,
               "signal_wait": waits, "slot_utilisation": slot_util,
               "kernels": {n: {"us": round(lper[n] * 1e3, 2), "algo_bytes": lbytes[n],
