@@ -53,7 +53,7 @@ FALLBACK_HBM_GBS = 6800.0
 # capture named in "source" (a T=1024 case of the same kernel, scaled to a full
 # launch by the rows it moves); null for kernels not captured since they changed.
 TRAFFIC = {
-    ("prefill", "permute"): {"bytes": 6.075e9,
+    ("prefill", "permute"): {"bytes": 6.073e9,
                              "source": "profiles/kernels_prefill_t1024_ncu_full.md (T=1024 capture x 4.024)"},
 }
 

@@ -24,7 +24,7 @@
 
 namespace ep {
 
-constexpr int kCombineThreads = 256;
+constexpr int kCombineThreads = 128;  // 4 warps: the grid spreads more evenly over the SMs than with 8
 constexpr int kCombineWarps = kCombineThreads / 32;
 
 __device__ __forceinline__ void bf16x8_to_f32(const int4& v, float* f) {
@@ -48,7 +48,7 @@ __device__ __forceinline__ int4 f32x8_to_bf16(const float* f) {
 
 // MODE 0: flat (rank partials), 1: hierarchical (rank, node, final), 2: low-latency (k order)
 template <int KMAX, int MODE, int U>
-__global__ void __launch_bounds__(kCombineThreads, KMAX <= 8 ? (U == 2 ? 2 : 3) : 1) combine_kernel(CombineArgs a) {
+__global__ void __launch_bounds__(kCombineThreads, (KMAX <= 8 ? (U == 2 ? 2 : 3) : 1) * (256 / kCombineThreads)) combine_kernel(CombineArgs a) {
     __shared__ int64_t sh_row[kCombineWarps][KMAX];
     __shared__ float sh_w[kCombineWarps][KMAX];
     __shared__ uint8_t sh_brk[kCombineWarps][KMAX];  // bit0: new rank group, bit1: new node group
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kCombineThreads, KMAX <= 8 ? (U == 2 ? 2 : 3) 
 }
 
 // vectors per lane per step for K <= 8: 2 (16 loads of 16 B in flight per
-// lane at 2 CTAs/SM of registers) beat 1 (8 loads at 3 CTAs/SM) on GB300:
+// lane at 16 warps/SM of registers) beat 1 (8 loads at 24 warps/SM) on GB300:
 // prefill combine 673 -> 649 us, hierarchical 2713 -> 2647 us.  Larger K
 // keeps 1 (the row arrays take the registers).
 static int combine_vectors(int mode) {
@@ -242,7 +242,7 @@ ep_status launch_combine(const CombineArgs& a, int mode, int num_sms, cudaStream
     // 1-2 slices 49 us, 7 slices 53 us, 8 slices 57 us).
     const int nvec = a.H / 8;
     const int vec = a.K <= 8 ? combine_vectors(mode) : 1;
-    const int64_t conc = (int64_t)num_sms * (vec == 2 ? 2 : 3) * kCombineWarps;  // resident warps
+    const int64_t conc = (int64_t)num_sms * (vec == 2 ? 2 : 3) * (256 / kCombineThreads) * kCombineWarps;  // resident warps
     int max_splits = nvec / 32 < 8 ? nvec / 32 : 8;
     if (max_splits < 1) max_splits = 1;
     int splits = max_splits;
@@ -260,7 +260,7 @@ ep_status launch_combine(const CombineArgs& a, int mode, int num_sms, cudaStream
     b.splits = splits;
     const int64_t items = n_tok * splits;
     int64_t want = (items + kCombineWarps - 1) / kCombineWarps;
-    const int64_t cap = (int64_t)num_sms * 16;
+    const int64_t cap = (int64_t)num_sms * 16 * (256 / kCombineThreads);
     const int grid = (int)(want < cap ? want : cap);
     cudaError_t e = mode == 0   ? launch_mode<0>(b, grid, vec, s)
                     : mode == 1 ? launch_mode<1>(b, grid, vec, s)
