@@ -41,6 +41,7 @@ struct ep_ll_buffer {
     int64_t wait_timeout_ns;
     int send_ctas_per_sm;    // send kernel launch shape
     size_t send_smem_bytes;
+    int recv_split;          // CTAs per (source, expert) region of the receive; 0 = from the region size
     int64_t* wait_trace;     // nullable device [E][R]: receive signal waits (ns)
 };
 
@@ -414,6 +415,8 @@ extern "C" ep_status ep_ll_buffer_create(const ep_config* cfg, int cap, ep_ll_bu
     b->send_smem_bytes = 72 * 1024;
     if (const char* v = getenv("EP_LL_SEND_CTAS_PER_SM")) b->send_ctas_per_sm = atoi(v) > 0 ? atoi(v) : 3;
     if (const char* v = getenv("EP_LL_SEND_SMEM_KB")) b->send_smem_bytes = (size_t)(atoi(v) > 16 ? atoi(v) : 72) * 1024;
+    b->recv_split = 0;
+    if (const char* v = getenv("EP_LL_RECV_SPLIT")) b->recv_split = atoi(v);
     {
         // room for two messages, the fixed part and at least two staged rows
         const size_t need = ll_send_fixed_smem(E) + 2 * (size_t)ep_ll_message_bytes(H) + 2 * (size_t)H * 2;
@@ -570,7 +573,7 @@ extern "C" ep_status ep_ll_recv(ep_ll_buffer* b, uint8_t* packed_x, float* packe
     // split a region's messages over Z CTAs when a full region is large (about
     // 512 KB per CTA), so hot experts do not serialise on one CTA
     int Z = (int)(((int64_t)b->cap * b->msg_bytes + (512 << 10) - 1) / (512 << 10));
-    if (const char* v = getenv("EP_LL_RECV_SPLIT")) Z = atoi(v);
+    if (b->recv_split > 0) Z = b->recv_split;
     if (Z < 1) Z = 1;
     if (Z > 8) Z = 8;
     lc.gridDim = dim3(a.R, a.E, Z);
