@@ -100,3 +100,60 @@ def test_low_latency_random_config(seed):
         orc.ll_combine(y, idx, w, sent["slot"], o_pk["layout_range"], R, E, cap, t0, n, out=o_out)
     buf.check()
     eq(out, o_out, "ll combine")
+
+
+def _wide_range_x(R, T, H, seed):
+    """bf16 rows whose 128-channel blocks span magnitudes from 2^-40 to 2^40
+    (power-of-two scalings of N(0,1), exact in bf16 above the subnormal range),
+    with some all-zero blocks, so that the FP8 scales cover many binades."""
+    x = inputs.random_x(R, T, H, seed).float()
+    rng = np.random.default_rng(seed + 11)
+    nb = H // 128
+    e = rng.integers(-40, 41, size=(R, T, nb)).astype(np.float64)
+    scale = np.exp2(e)
+    scale[rng.random((R, T, nb)) < 0.05] = 0.0
+    s = torch.from_numpy(np.repeat(scale, 128, axis=2)).float()
+    return (x * s).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("seed", SEEDS[:12])
+def test_fp8_random_config(seed):
+    """The FP8 rows from the quantiser, the one-pass dispatch into the permuted
+    layout and the one-pass dispatch into the receive layout, on random
+    configurations with block maxima over many binades, against the oracle's
+    quantiser row by row."""
+    rng = np.random.default_rng(seed + 3)
+    R = int(rng.choice([1, 2, 4, 8]))
+    E = R * int(rng.choice([1, 2, 4, 8]))
+    K = int(rng.integers(1, min(E, 8) + 1))
+    T = int(rng.choice([1, 7, 33, 130]))
+    H = int(rng.choice([128, 256, 384, 1024, 2048]))
+    C = int(rng.integers(1, 5))
+    mask_p = float(rng.choice([0.0, 0.1]))
+    idx = inputs.random_topk(R, E, K, T, seed, mask_p)
+    x = _wide_range_x(R, T, H, seed)
+    w = inputs.random_weights(R, T, K, seed)
+    ctx = Context(R, E, K, T, H, num_channels=C)
+    xd, idxd, wd = x.cuda(), idx.cuda(), w.cuda()
+    h = ctx.notify_dispatch(idxd, ctx.get_dispatch_layout(idxd))
+    n_def = H + H // 32
+    xb = bits(x).reshape(R * T, H)
+    o_rows = np.zeros((R * T, n_def), np.uint8)
+    for g in range(R * T):
+        codes, scales = orc.quantize_row(xb[g])
+        o_rows[g, :H] = codes
+        o_rows[g, H:] = scales.view(np.uint8)
+    xq = ctx.quantize_fp8(xd)
+    perm = ctx.dispatch_permuted_quant(xd, idxd, wd, h)
+    recv = ctx.dispatch_quant(xd, idxd, wd, h)
+    ctx.check()
+    eq(bits(xq)[:, :n_def], o_rows, "quantised rows")
+    pp = h["perm_pos"].cpu().numpy().reshape(R * T, K)
+    got = bits(perm["permuted_xq"])
+    for g, k in zip(*np.nonzero(pp >= 0)):
+        eq(got[pp[g, k], :n_def], o_rows[g], f"permuted row of token {g}, entry {k}")
+    sp = h["send_pos"].cpu().numpy().reshape(R * T, R)
+    rb = h["rank_base"].cpu().numpy()
+    gr = bits(recv["recv_xq"])
+    for g, d in zip(*np.nonzero(sp >= 0)):
+        eq(gr[rb[d] + sp[g, d], :n_def], o_rows[g], f"received row of token {g} at rank {d}")
