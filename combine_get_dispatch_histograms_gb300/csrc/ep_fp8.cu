@@ -270,11 +270,17 @@ extern "C" ep_status ep_quantize_fp8(ep_ctx* c, const void* x, uint8_t* xq, void
     // one wave of resident CTAs
     const int64_t total = tokens * (c->cfg.hidden / 16);
     const bool narrow = total <= (int64_t)UINT32_MAX - 2 * kQuantU * 256 * (int64_t)c->num_sms * 8;
-    int per_sm = 0;
-    EP_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &per_sm, narrow ? quantize_rows_kernel<uint32_t> : quantize_rows_kernel<uint64_t>, 256, 0));
-    if (per_sm < 1) per_sm = 1;
-    if (per_sm > 8) per_sm = 8;
+    // resident CTAs per SM, queried once per device and index width
+    static int cached[kMaxDevicesTracked][2] = {};
+    const bool cacheable = c->device >= 0 && c->device < kMaxDevicesTracked;
+    int per_sm = cacheable ? cached[c->device][narrow] : 0;
+    if (per_sm == 0) {
+        EP_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, narrow ? quantize_rows_kernel<uint32_t> : quantize_rows_kernel<uint64_t>, 256, 0));
+        if (per_sm < 1) per_sm = 1;
+        if (per_sm > 8) per_sm = 8;
+        if (cacheable) cached[c->device][narrow] = per_sm;
+    }
     int64_t grid = (int64_t)c->num_sms * per_sm;
     if (grid > (total + 255) / 256) grid = (total + 255) / 256;
     const uint16_t* xb = static_cast<const uint16_t*>(x);
