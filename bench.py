@@ -477,6 +477,32 @@ def main():
                                        "frac": round(fb / (fd * 1e-3) / 1e9 / peak0, 3)}}
         del fperm
 
+    # ---- expert-aligned permute: every (rank, expert) block rounded up to 128 rows ----
+    aligned = None
+    if not hier:
+        actx = Context(R, E, K, T, H, num_channels=C, expert_alignment=128)
+        ah = actx.notify_dispatch(idx_d, actx.get_dispatch_layout(idx_d))  # the receive layout is the same
+        aperm = dict(permuted_x=torch.empty(ah.num_perm_rows, H, dtype=torch.bfloat16, device="cuda"),
+                     perm_src_row=torch.empty(ah.num_perm_rows, dtype=torch.int32, device="cuda"))
+        for _ in range(args.warmup):
+            flush()
+            actx.permute(ah, recv, out=aperm)
+        aev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush()
+            aev[i][0].record(stream)
+            actx.permute(ah, recv, out=aperm)
+            aev[i][1].record(stream)
+        torch.cuda.synchronize()
+        actx.check()
+        ad = statistics.median(e[0].elapsed_time(e[1]) for e in aev)
+        ab = (copies + pairs) * 2 * H  # padding rows are not written
+        peak0, _ = measured_hbm_gbs()
+        aligned = {"alignment": 128, "permuted_rows": ah.num_perm_rows, "pairs": pairs,
+                   "permute": {"us": round(ad * 1e3, 2), "algo_bytes": ab, "GBps": round(ab / (ad * 1e-3) / 1e9, 1),
+                               "frac": round(ab / (ad * 1e-3) / 1e9 / peak0, 3)}}
+        del aperm, actx
+
     # ---- the same steps without a host synchronisation, replayed as one CUDA graph ----
     # (notify's no-wait form; buffers sized for the worst case; the kernels read
     # the row totals from the handle on the device)
@@ -1022,6 +1048,7 @@ def main():
         "wall_s_timed_region": round(wall, 4),
         "ll_decode": ll,
         "fused_path": fused,
+        "expert_aligned": aligned,
         "graph": nw_graph,
         "fp8_rows": fp8,
     }
