@@ -68,6 +68,19 @@ class Handle(dict):
     """Device arrays of the dispatch handle plus the host counts of notify."""
 
     _cs = None
+    _hrecv = None  # host arrays the waiting notify writes (owned by this handle)
+    _hexp = None
+    synced = False
+
+    @property
+    def host_num_recv_tokens(self):
+        """[R] rows each receiver gets (waiting notify only, else None)."""
+        return self._hrecv[:] if self.synced and self._hrecv is not None else None
+
+    @property
+    def host_num_recv_per_expert(self):
+        """[R*L] pairs of each (receiver, local expert) (waiting notify only, else None)."""
+        return self._hexp[:] if self.synced and self._hexp is not None else None
 
     def __setitem__(self, key, value):
         self._cs = None
@@ -203,7 +216,10 @@ class Context:
         h = handle if handle is not None else self.alloc_handle()
         cs = h.c_struct()
         if wait:
-            host_recv, host_exp, host_tot = self._host_recv, self._host_exp, self._host_tot
+            if h._hrecv is None:  # the handle's own host arrays: no copy after the wait
+                h._hrecv = (ctypes.c_int32 * self.R)()
+                h._hexp = (ctypes.c_int32 * self.E)()
+            host_recv, host_exp, host_tot = h._hrecv, h._hexp, self._host_tot
         else:
             host_recv = host_exp = host_tot = None
         nodes = self.N > 1 or fn == "ep_notify_dispatch"
@@ -214,12 +230,8 @@ class Context:
             _stream(stream)))
         h.synced = wait
         if wait:
-            # copies of the host counts (the arrays are reused by the next notify)
-            h.host_num_recv_tokens = host_recv[:]
-            h.host_num_recv_per_expert = host_exp[:]
             h.num_recv_rows, h.num_perm_rows, h.num_stage_rows = host_tot
         else:
-            h.host_num_recv_tokens = h.host_num_recv_per_expert = None
             h.num_recv_rows, h.num_perm_rows, h.num_stage_rows = self.max_rows
         return h
 
