@@ -41,7 +41,8 @@ struct ep_ll_buffer {
     int64_t wait_timeout_ns;
     int send_ctas_per_sm;    // send kernel launch shape
     size_t send_smem_bytes;
-    int recv_split;          // CTAs per (source, expert) region of the receive; 0 = from the region size
+    int recv_split;          // CTAs per (source, expert) region of the receive; 0 = from the last send
+    int last_send_n;         // tokens per source of the last send (sizes the receive's split)
     int64_t* wait_trace;     // nullable device [E][R]: receive signal waits (ns)
 };
 
@@ -416,6 +417,7 @@ extern "C" ep_status ep_ll_buffer_create(const ep_config* cfg, int cap, ep_ll_bu
     if (const char* v = getenv("EP_LL_SEND_CTAS_PER_SM")) b->send_ctas_per_sm = atoi(v) > 0 ? atoi(v) : 3;
     if (const char* v = getenv("EP_LL_SEND_SMEM_KB")) b->send_smem_bytes = (size_t)(atoi(v) > 16 ? atoi(v) : 72) * 1024;
     b->recv_split = 0;
+    b->last_send_n = cap;
     if (const char* v = getenv("EP_LL_RECV_SPLIT")) b->recv_split = atoi(v);
     {
         // room for two messages, the fixed part and at least two staged rows
@@ -509,6 +511,7 @@ extern "C" ep_status ep_ll_send(ep_ll_buffer* b, const void* x, const int64_t* t
     a.cap = b->cap;
     a.t0 = t0;
     a.n = n;
+    b->last_send_n = n;
     a.msg_bytes = b->msg_bytes;
     a.status = b->status;
     cudaStream_t s = as_stream(stream);
@@ -570,9 +573,12 @@ extern "C" ep_status ep_ll_recv(ep_ll_buffer* b, uint8_t* packed_x, float* packe
     a.status = b->status;
     a.wait_trace = b->wait_trace;
     cudaLaunchConfig_t lc = {};
-    // split a region's messages over Z CTAs when a full region is large (about
-    // 512 KB per CTA), so hot experts do not serialise on one CTA
-    int Z = (int)(((int64_t)b->cap * b->msg_bytes + (512 << 10) - 1) / (512 << 10));
+    // split each region's messages over Z CTAs, Z = half the average messages
+    // per region of the last send (ceil(n*K/E)), rounded up: the measured best
+    // on the decode batch (4 messages per region on average: Z = 2) and on the
+    // Zipf-skewed microbatches (8 on average, hot regions near cap: Z = 4)
+    const int64_t avg = ((int64_t)b->last_send_n * f.num_topk + f.num_experts - 1) / f.num_experts;
+    int Z = (int)((avg + 1) / 2);
     if (b->recv_split > 0) Z = b->recv_split;
     if (Z < 1) Z = 1;
     if (Z > 8) Z = 8;
