@@ -41,8 +41,8 @@ __device__ __forceinline__ float div_by_scale(float x, float scale, float y) {
     return __fmaf_rn(-r, y, q0);
 }
 
-// Scales below this (block maxima under ~3.5e-28) and non-finite ones take
-// the IEEE division instruction sequence per element instead.
+// Scales below this (block maxima under ~3.5e-28) and non-finite ones divide
+// each element with __fdiv_rn instead.
 constexpr float kRcpScaleMin = 0x1p-100f;
 constexpr float kRcpScaleMax = 3.0e38f;
 

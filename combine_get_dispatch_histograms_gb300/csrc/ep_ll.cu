@@ -13,8 +13,8 @@
 // indices).
 //
 // GB300 design on one GPU: the R ranks' regions are one allocation; the send
-// kernel quantises each token once (per-128-channel amax, IEEE division,
-// cvt.rn.satfinite.e4m3x2) and stores the message to its K regions; slots are
+// kernel quantises each token once (per-128-channel amax, the e4m3 code of the
+// IEEE quotient x / scale, ep_fp8.cuh) and stores the message to its K regions; slots are
 // the deterministic (t, k)-order rank of the entry among the source's entries
 // for the same expert (no atomic slot claims); a publisher kernel, launched as
 // a programmatic dependent of the send, stores every count of every source
