@@ -186,3 +186,29 @@ def test_no_wait_small_buffers_flag_capacity():
     assert e.value.status == "EP_ERR_CAPACITY"
     o_perm = orc.permute(idx, o_disp["recv_x"], o_note, R, E)
     eq(fused["permuted_x"], o_perm["permuted_x"][:npm - 1], "permuted_x (rows that fit)")
+
+
+def test_handle_host_counts_follow_each_notify():
+    """A handle's host counts are those of the last notify on it: a waiting
+    notify fills them, a no-wait one clears them, and another handle's notify
+    leaves them alone (each handle owns its host arrays)."""
+    R, E, K, T, H = 4, 16, 4, 120, 64
+    idx1 = inputs.random_topk(R, E, K, T, 50, 0.1)
+    idx2 = inputs.random_topk(R, E, K, T, 51, 0.0)
+    ctx = Context(R, E, K, T, H, num_channels=2)
+    n1 = orc.notify(orc.layout(idx1, R, E), R, E, T, 2)
+    n2 = orc.notify(orc.layout(idx2, R, E), R, E, T, 2)
+    i1, i2 = idx1.cuda(), idx2.cuda()
+    l1, l2 = ctx.get_dispatch_layout(i1), ctx.get_dispatch_layout(i2)
+    h = ctx.alloc_handle()
+    ctx.notify_dispatch(i1, l1, handle=h)
+    assert list(h.host_num_recv_tokens) == list(n1["num_recv_tokens"])
+    assert list(h.host_num_recv_per_expert) == list(n1["num_recv_per_expert"].reshape(-1))
+    ctx.notify_dispatch(i2, l2, handle=h, wait=False)
+    assert h.host_num_recv_tokens is None and h.host_num_recv_per_expert is None
+    ctx.notify_dispatch(i2, l2, handle=h)
+    assert list(h.host_num_recv_tokens) == list(n2["num_recv_tokens"])
+    assert h.num_recv_rows == int(n2["rank_base"][R])
+    other = ctx.notify_dispatch(i1, l1)
+    assert list(other.host_num_recv_tokens) == list(n1["num_recv_tokens"])
+    assert list(h.host_num_recv_tokens) == list(n2["num_recv_tokens"])
