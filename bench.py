@@ -7,7 +7,11 @@ H=7168 bf16): layout -> notify (with its host sync) -> dispatch scatter ->
 permute -> combine, with the identity expert (expert_out = permuted_x).
 The same run also times the low-latency layer on the decode workload
 (R=16 x 128 tokens, FP8 send + receive/pack + BF16 combine) and reports it
-as ``ll_decode``.
+as ``ll_decode``.  Further legs of the same line: ``fused_path`` (dispatch
+straight into the per-expert layout), ``expert_aligned`` (the permute into
+128-row aligned blocks), ``graph`` (the steps without a host wait, each one
+CUDA graph), ``fp8_rows`` (FP8 quantiser and FP8 dispatches) and ``e2e``
+(the step from pinned host buffers, copies inside the timed region).
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 a bounded sample of the same workload instead.
