@@ -43,6 +43,7 @@ SIGNATURES = {
     "ep_ctx_check": (INT, [P, P]),
     "ep_ctx_set_wait_timeout_us": (INT, [P, I64]),
     "ep_ctx_set_expert_alignment": (INT, [P, INT]),
+    "ep_ctx_expert_alignment": (I32, [P]),
     "ep_ctx_last_launches": (I32, [P]),
     "ep_get_dispatch_layout": (INT, [P, P, P, P, P, P, P, P]),
     "ep_get_dispatch_layout_noalloc": (INT, [I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P]),

@@ -257,7 +257,7 @@ __device__ void notify_global_scan(const NotifyArgs& a, int32_t* sh /* >= 2E + 3
     // thread; each expert's block takes its count rounded up to the alignment
     const int per = (E + blockDim.x - 1) / blockDim.x;
     const int e0 = threadIdx.x * per;
-    const int al = a.align;
+    const int al = a.align > 1 ? a.align : 1;
     auto rows_of = [al](int32_t n) -> int32_t { return (n + al - 1) / al * al; };
     int32_t local = 0;
     for (int e = e0; e < e0 + per && e < E; ++e) local += rows_of(tot[e]);
@@ -602,10 +602,9 @@ extern "C" ep_status ep_ctx_create(const ep_config* cfg, ep_ctx** out) {
     *out = nullptr;
     ep_status st = validate_config(cfg);
     if (st != EP_OK) return st;
-    ep_ctx* c = new ep_ctx();
-    c->totals_known = true;  // nothing notified yet: zero rows
+    ep_ctx* c = new ep_ctx();  // value-initialised: every member starts at zero
+    c->totals_known = true;      // nothing notified yet: zero rows, so a copy launched now does nothing
     c->expert_alignment = 1;
-    std::memset(c, 0, sizeof(*c));
     c->cfg = *cfg;
     c->L = cfg->num_experts / cfg->num_ranks;
     c->G = cfg->num_ranks / cfg->num_nodes;
@@ -697,6 +696,8 @@ extern "C" ep_status ep_ctx_set_expert_alignment(ep_ctx* c, int32_t alignment) {
     c->expert_alignment = alignment;
     return EP_OK;
 }
+
+extern "C" int32_t ep_ctx_expert_alignment(const ep_ctx* c) { return c ? c->expert_alignment : 0; }
 
 extern "C" int32_t ep_ctx_last_launches(const ep_ctx* c) { return c ? c->last_launches : 0; }
 

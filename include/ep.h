@@ -105,6 +105,9 @@ ep_status ep_ctx_set_wait_timeout_us(ep_ctx* ctx, int64_t us);
  * order; padding rows of permuted_x, perm_src_row, perm_src_token and
  * perm_weight are not written.  Combine reads only the pairs' rows. */
 ep_status ep_ctx_set_expert_alignment(ep_ctx* ctx, int32_t alignment);
+/* The context's current expert alignment (1 for a fresh context); 0 if ctx
+ * is NULL. */
+int32_t ep_ctx_expert_alignment(const ep_ctx* ctx);
 
 /* Number of kernel launches the last call on this context made (for the
  * bench's launch count). */
@@ -149,7 +152,10 @@ ep_status ep_get_dispatch_layout(ep_ctx* ctx, const int64_t* topk_idx,
  *     and launches nothing (use ep_get_dispatch_layout instead).
  *   - status_out (device, nullable): if given, the kernel ORs its error bits
  *     into it (1 = a topk_idx value outside [-1, E) was skipped); the caller
- *     zeroes it.
+ *     zeroes it.  If NULL, the error bits go to a word of the shared scratch
+ *     that no caller can read and the next call clears: an out-of-range
+ *     topk_idx value is then skipped silently.  Pass status_out whenever the
+ *     routing is not known to be valid.
  *   - The first call on a device looks up the scratch array's device address
  *     (once per device, with that device current); make that first call before
  *     any stream capture.  Every call clears the counters it needs before its

@@ -106,3 +106,24 @@ def test_aligned_fp8_rows():
     eq(bits(permq["permuted_xq"][:P])[used], recv_rows[src], "permuted FP8 rows")
     tok = bits(fusedq["perm_src_token"][:P])[used]
     eq(bits(fusedq["permuted_xq"][:P])[used], xq_np[tok], "fused FP8 rows")
+
+
+def test_fresh_context_has_alignment_one_and_nothing_notified():
+    """A fresh context starts with expert alignment 1 (no padding) and with
+    zero known rows, so a copy launched before any notify does nothing."""
+    R, E, K, T, H = 4, 8, 2, 16, 128
+    ctx = Context(R, E, K, T, H)
+    assert ctx.lib.ep_ctx_expert_alignment(ctx._ctx) == 1
+    ctx.set_expert_alignment(16)
+    assert ctx.lib.ep_ctx_expert_alignment(ctx._ctx) == 16
+    ctx.set_expert_alignment(1)
+    assert ctx.lib.ep_ctx_expert_alignment(ctx._ctx) == 1
+    # the default alignment gives the oracle's unpadded offsets
+    idx = inputs.random_topk(R, E, K, T, 3, 0.1)
+    fresh = Context(R, E, K, T, H)
+    lay = fresh.get_dispatch_layout(idx.cuda())
+    h = fresh.notify_dispatch(idx.cuda(), lay)
+    torch.cuda.synchronize()
+    o_note = orc.notify(orc.layout(idx, R, E), R, E, T, 8)
+    for k in ("expert_offsets", "perm_rank_base"):
+        eq(h[k], o_note[k], k)
