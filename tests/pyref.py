@@ -195,3 +195,43 @@ def bf16_bits_of(v) -> int:
 
 def bf16_value(bits: int) -> float:
     return struct.unpack("<f", struct.pack("<I", (int(bits) & 0xFFFF) << 16))[0]
+
+
+# ---------------------------------------------------------------------------
+# low-latency pack and combine, written from the definitions
+# ---------------------------------------------------------------------------
+
+def ll_packed_rows(valid, R, E, T, K, t0, n):
+    """Where every valid (s, t, k) of the microbatch [t0, t0 + n) sits in the
+    packed per-expert layout: {(s, t, k): (d, l, row)}, row counted inside
+    expert (d, l)'s block.  Sources are laid out one after another in s order,
+    and inside a source the entries keep their (t, k) order."""
+    L = E // R
+    slot, counts = ll_slots(valid, R, E, T, K, t0, n)
+    where = {}
+    for (s, t, k), i in slot.items():
+        e = valid[(s, t, k)]
+        before = sum(counts.get((s2, e), 0) for s2 in range(s))
+        where[(s, t, k)] = (e // L, e % L, before + i)
+    return where
+
+
+def ll_combine_exact(y_rows, where, idx, w, t0, n):
+    """out[s][t] as exact bf16 bits: for k ascending over the valid entries,
+    acc = fma(w, y, acc) rounded once to fp32 per step, then bf16 (nearest,
+    ties to even).  y_rows maps (d, l, row) to a list of fp32 values (one per
+    channel); returns {(s, t): [bits per channel]} for tokens of the batch."""
+    R, T, K = idx.shape
+    out = {}
+    H = len(next(iter(y_rows.values()))) if y_rows else 0
+    for s in range(R):
+        for t in range(t0, t0 + n):
+            ks = [k for k in range(K) if (s, t, k) in where]
+            vals = []
+            for j in range(H):
+                acc = 0.0
+                for k in ks:
+                    acc = fmaf(float(w[s, t, k]), y_rows[where[(s, t, k)]][j], acc)
+                vals.append(bf16_bits_of(acc))
+            out[(s, t)] = vals
+    return out

@@ -14,7 +14,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "ep_oracle.c")
 PIN_TESTS = ["tests/test_oracle_worked.py", "tests/test_oracle_order.py", "tests/test_oracle_invariants.py",
-             "tests/test_oracle_fp8.py", "tests/test_oracle_bruteforce.py"]
+             "tests/test_oracle_fp8.py", "tests/test_oracle_bruteforce.py", "tests/test_oracle_ll_hier.py"]
 
 # (name, original text, mutated text)
 MUTANTS = [
@@ -61,6 +61,24 @@ MUTANTS = [
      "acc += round_up(n, align);", "acc += n;"),
     ("aligned permute places a block at its unpadded start",
      "row += padded;\n        i = j;", "row += cnt;\n        i = j;"),
+    ("low-latency combine multiply and add rounded separately",
+     "acc = fmaf(w[tok * K + k], orc_bf16_to_f32(y_ll[row * H + j]), acc);",
+     "{ volatile float pr = w[tok * K + k] * orc_bf16_to_f32(y_ll[row * H + j]); acc = pr + acc; }"),
+    ("low-latency combine in descending k order",
+     "for (int k = 0; k < K; ++k) {\n                    int64_t e = topk_idx[tok * K + k];\n"
+     "                    if (e < 0 || e >= E) continue;\n                    int d = (int)(e / L), l = (int)(e % L);",
+     "for (int k = K - 1; k >= 0; --k) {\n                    int64_t e = topk_idx[tok * K + k];\n"
+     "                    if (e < 0 || e >= E) continue;\n                    int d = (int)(e / L), l = (int)(e % L);"),
+    ("low-latency combine ignores the source's begin in the packed block",
+     "int64_t row = ((int64_t)d * L + l) * per_expert + begin + slot[tok * K + k];",
+     "int64_t row = ((int64_t)d * L + l) * per_expert + slot[tok * K + k]; (void)begin;"),
+    ("dequantisation with the first block's scale for every block",
+     "scales[r * S + j / 128]", "scales[r * S]"),
+    ("stage B forwards the row at its offset inside the home rank's block",
+     "staging + (int64_t)i * H,", "staging + (int64_t)(i - stage_base[h]) * H,"),
+    ("stage A reads the source token with transposed indices",
+     "memcpy(staging + (int64_t)p * H, x + ((int64_t)s * T + t) * H,",
+     "memcpy(staging + (int64_t)p * H, x + ((int64_t)t * R + s) * H,"),
 ]
 
 
