@@ -157,3 +157,24 @@ def random_weights(R: int, T: int, K: int, seed: int) -> torch.Tensor:
 def random_x(R: int, T: int, H: int, seed: int) -> torch.Tensor:
     g = torch.Generator().manual_seed(seed + 11)
     return torch.randn(R, T, H, generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def random_rows(n: int, H: int, seed: int, device: Optional[str] = None) -> torch.Tensor:
+    """[n][H] bf16: N(0, 1) values times a per-row power of two in 2^-4..2^4.
+
+    A stand-in expert output with a different row for every permuted row or
+    packed slot (unlike the identity expert, whose rows repeat the token's x
+    for every k), so that a combine reading the wrong row of a token changes
+    its result.  Drawn like ``make_x`` (CPU generator, or a seeded CUDA
+    generator in slabs when ``device`` is a CUDA device)."""
+    on_cpu = device is None or device == "cpu"
+    g = torch.Generator(device="cpu" if on_cpu else device).manual_seed(seed + 23)
+    dev = "cpu" if on_cpu else device
+    out = torch.empty(n, H, dtype=torch.bfloat16, device=dev)
+    step = max(1, (1 << 26) // max(1, H))
+    for i in range(0, n, step):
+        j = min(n, i + step)
+        v = torch.randn(j - i, H, generator=g, device=dev, dtype=torch.float32)
+        e = torch.randint(-4, 5, (j - i, 1), generator=g, device=dev).to(torch.float32)
+        out[i:j] = (v * torch.exp2(e)).to(torch.bfloat16)
+    return out

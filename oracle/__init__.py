@@ -170,6 +170,19 @@ def quantize_row(x_bits: np.ndarray):
     return codes, scales
 
 
+def quantize_rows(x_bits: np.ndarray):
+    """quantize_row over every row of a [N][H] array (a loop of single-row
+    calls: the codes and scales of each row depend on that row alone)."""
+    x_bits = _np(x_bits, np.uint16)
+    n, H = x_bits.shape
+    codes = np.empty((n, H), np.uint8)
+    scales = np.empty((n, H // 128), np.float32)
+    f = lib().orc_quantize_row
+    for i in range(n):
+        f(_p(x_bits[i]), H, _p(codes[i]), _p(scales[i]))
+    return codes, scales
+
+
 # ---------------------------------------------------------------------------
 # normal (high-throughput) mode
 # ---------------------------------------------------------------------------

@@ -4,7 +4,7 @@ import numpy as np
 import torch
 
 import oracle as orc
-from combine_get_dispatch_histograms_gb300 import Context, LLBuffer
+from combine_get_dispatch_histograms_gb300 import Context, LLBuffer, inputs
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
@@ -91,6 +91,17 @@ def compare_normal(R, E, K, T, H, C, x, idx, w, nodes=1, hier=False):
         o_out = orc.combine(o_perm["permuted_x"], o_perm["perm_pos"], idx, w, R, E, "ord32")
     eq(out, o_out, "combine (fp32 order)")
     check_tolerance(out, orc.combine(o_perm["permuted_x"], o_perm["perm_pos"], idx, w, R, E, "ref64"))
+    # an expert output with a different row for every permuted row: a combine
+    # that reads another pair's row of the same token changes the bits
+    y = inputs.random_rows(int(o_perm["permuted_x"].shape[0]), H, seed=int(T) * 131 + R)
+    out_y = ctx.combine(h, y.cuda(), idx.cuda(), w.cuda(), hier=hier)
+    ctx.check()
+    if hier:
+        o_y = orc.combine_hier(y, o_perm["perm_pos"], idx, w, R, E, nodes)
+    else:
+        o_y = orc.combine(y, o_perm["perm_pos"], idx, w, R, E, "ord32")
+    eq(out_y, o_y, "combine of distinct expert rows (fp32 order)")
+    check_tolerance(out_y, orc.combine(y, o_perm["perm_pos"], idx, w, R, E, "ref64"))
     return ctx
 
 

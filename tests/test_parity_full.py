@@ -5,9 +5,12 @@ The oracle computes every integer result exactly at full size (layout, notify,
 handle, positions, slots, counts; its copy steps run on an 8-channel stand-in
 of x, since positions do not depend on H).  Row data is checked for every row
 against the row the oracle assigned (a GPU gather of x does the data movement
-of the comparison); combine outputs are checked bit-exactly on sampled tokens,
-each computed by the oracle on a sub-problem holding only those tokens with
-the same experts, weights and summation order."""
+of the comparison); every FP8 row and message is checked against the oracle's
+quantisation of its source token.  Combine outputs are checked bit-exactly on
+sampled tokens, each computed by the oracle on a sub-problem holding only
+those tokens with the same experts, weights and summation order, for the
+identity expert and for an expert output with a distinct row per permuted
+row or packed slot."""
 import numpy as np
 import pytest
 import torch
@@ -21,16 +24,48 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 N_SAMPLES = 384
 
 
-def _rows_equal(got: torch.Tensor, src: torch.Tensor, src_rows: np.ndarray, what: str, chunk=1 << 15):
-    """got[i] == src[src_rows[i]] for every i (compared on the GPU, in chunks)."""
-    assert got.shape[0] == len(src_rows), what
+def _rows_equal(got: torch.Tensor, src: torch.Tensor, src_rows: np.ndarray, what: str, chunk=1 << 15,
+                got_rows: np.ndarray = None):
+    """got[i] == src[src_rows[i]] for every i, or got[got_rows[i]] ==
+    src[src_rows[i]] when got_rows is given (compared byte for byte on the
+    GPU, in chunks)."""
+    if got_rows is None:
+        assert got.shape[0] == len(src_rows), what
+    else:
+        assert len(got_rows) == len(src_rows), what
+        gidx = torch.from_numpy(got_rows.astype(np.int64)).to(got.device)
     idx = torch.from_numpy(src_rows.astype(np.int64)).to(got.device)
     for a in range(0, len(src_rows), chunk):
         b = min(len(src_rows), a + chunk)
-        exp = src.index_select(0, idx[a:b])
-        if not torch.equal(got[a:b].view(torch.int16), exp.view(torch.int16)):
-            bad = (got[a:b].view(torch.int16) != exp.view(torch.int16)).any(dim=1).nonzero()
+        exp = src.index_select(0, idx[a:b]).contiguous().view(torch.uint8)
+        g = (got[a:b] if got_rows is None else got.index_select(0, gidx[a:b])).contiguous().view(torch.uint8)
+        if not torch.equal(g, exp):
+            bad = (g != exp).any(dim=1).nonzero()
             raise AssertionError(f"{what}: row {a + int(bad[0])} differs ({len(bad)} rows in chunk)")
+
+
+def _oracle_fp8_rows(xf: torch.Tensor) -> torch.Tensor:
+    """The oracle's FP8 row (H codes, then H/128 fp32 scales as bytes) of
+    every token of xf [N][H], on the GPU for the gathers."""
+    codes, scales = orc.quantize_rows(bits(xf))
+    return torch.from_numpy(np.concatenate([codes, scales.view(np.uint8)], axis=1)).to(xf.device)
+
+
+def _combine_sub_problem(y_rows: np.ndarray, idx_np, w_np, g, R, E, K, hier, N):
+    """The oracle's combine of the sampled tokens g: one sub-problem holding
+    only those tokens (on source 0) with their experts, weights and the rows
+    y_rows [m][K][H] their entries read (rows of masked entries unused)."""
+    m = len(g)
+    H = y_rows.shape[2]
+    sub_idx = np.full((R, m, K), -1, np.int64)
+    sub_w = np.zeros((R, m, K), np.float32)
+    sub_idx[0], sub_w[0] = idx_np[g], w_np[g]
+    sub_pp = np.full((R, m, K), -1, np.int32)
+    sub_pp[0] = (np.arange(m)[:, None] * K + np.arange(K)[None, :]).astype(np.int32)
+    y_sub = y_rows.reshape(m * K, H)
+    if hier:
+        return orc.combine_hier(y_sub, sub_pp, sub_idx, sub_w, R, E, N)[0]
+    return orc.combine(y_sub, sub_pp, sub_idx, sub_w, R, E, "ord32")[0]
 
 
 def _normal_full(wl, hier: bool):
@@ -90,20 +125,24 @@ def _normal_full(wl, hier: bool):
     rng = np.random.default_rng(7)
     g = rng.choice(R * T, size=min(N_SAMPLES, R * T), replace=False)
     m = len(g)
+    gd = torch.from_numpy(g).cuda()
     idx_np, w_np = idx.numpy().reshape(R * T, K), w.numpy().reshape(R * T, K)
-    sub_idx = np.full((R, m, K), -1, np.int64)
-    sub_w = np.zeros((R, m, K), np.float32)
-    sub_idx[0], sub_w[0] = idx_np[g], w_np[g]
-    sub_pp = np.full((R, m, K), -1, np.int32)
-    sub_pp[0] = (np.arange(m)[:, None] * K + np.arange(K)[None, :]).astype(np.int32)
-    xs = bits(xf.index_select(0, torch.from_numpy(g).cuda()))          # identity expert: rows are x
-    y_sub = np.repeat(xs, K, axis=0)
-    if hier:
-        exp = orc.combine_hier(y_sub, sub_pp, sub_idx, sub_w, R, E, N)[0]
-    else:
-        exp = orc.combine(y_sub, sub_pp, sub_idx, sub_w, R, E, "ord32")[0]
-    got = bits(out.view(R * T, H).index_select(0, torch.from_numpy(g).cuda()))
+    xs = bits(xf.index_select(0, gd))          # identity expert: every entry's row is x
+    exp = _combine_sub_problem(np.repeat(xs[:, None, :], K, axis=1), idx_np, w_np, g, R, E, K, hier, N)
+    got = bits(out.view(R * T, H).index_select(0, gd))
     eq(got, exp, "combine (sampled tokens)")
+    # an expert output with a distinct row per permuted row: each entry of a
+    # sampled token reads its own row, located by the oracle's perm_pos
+    P = int(o_note["perm_rank_base"][R])
+    del perm, out
+    y = inputs.random_rows(P, H, seed=99, device="cuda")
+    out_y = ctx.combine(h, y, idxd, wd, hier=hier)
+    ctx.check()
+    pp = o_perm["perm_pos"].reshape(R * T, K)[g]
+    rows = bits(y.index_select(0, torch.from_numpy(np.maximum(pp, 0).reshape(-1)).cuda().long()))
+    exp = _combine_sub_problem(rows.reshape(m, K, H), idx_np, w_np, g, R, E, K, hier, N)
+    got = bits(out_y.view(R * T, H).index_select(0, gd))
+    eq(got, exp, "combine of distinct expert rows (sampled tokens)")
     return ctx
 
 
@@ -128,10 +167,14 @@ def _ll_full(wl):
     buf = LLBuffer(R, E, K, T, H, cap)
     idxd, wd = idx.cuda(), w.cuda()
     out = torch.zeros(R, T, H, dtype=torch.bfloat16, device="cuda")
+    out_y = torch.zeros(R, T, H, dtype=torch.bfloat16, device="cuda")
     pk = buf.alloc_packed()
     y_ll = torch.empty(pk["packed_x"].shape, dtype=torch.bfloat16, device="cuda")
+    y_rand = inputs.random_rows(R * L * R * cap, H, seed=77, device="cuda").view(y_ll.shape)
+    q = _oracle_fp8_rows(xf)                    # every token's codes and scales, by the oracle
     probe = np.zeros((R, T, 128), np.uint16)
     rng = np.random.default_rng(11)
+    idx_np, w_np = idx.numpy(), w.numpy()
     for t0 in range(0, T, cap):
         n = min(cap, T - t0)
         buf.dispatch(x, idxd, t0, n, out=pk)
@@ -141,6 +184,7 @@ def _ll_full(wl):
             y_ll[d] = (pk["packed_x"][d].view(torch.float8_e4m3fn).float() *
                        pk["packed_scales"][d].repeat_interleave(128, dim=-1)).to(torch.bfloat16)
         buf.combine(y_ll, idxd, wd, pk, t0, n, out=out)
+        buf.combine(y_rand, idxd, wd, pk, t0, n, out=out_y)
         buf.check()
         # integers exactly (slots do not depend on H: the oracle runs on a 128-channel stand-in)
         sent = orc.ll_send(probe, idx, R, E, cap, t0, n)
@@ -148,42 +192,52 @@ def _ll_full(wl):
         eq(pk["slot"][:, t0:t0 + n], sent["slot"][:, t0:t0 + n], "slot")
         eq(pk["packed_recv_count"], o_pk["packed_recv_count"], "packed_recv_count")
         eq(pk["layout_range"], o_pk["layout_range"], "layout_range")
-        # sampled messages: codes, scales and source of valid (s, t, k)
-        s_, t_, k_ = np.nonzero(idx.numpy()[:, t0:t0 + n] >= 0)
-        pick = rng.choice(len(s_), size=min(N_SAMPLES, len(s_)), replace=False)
+        # every message of the microbatch: codes, scales and source of each valid (s, t, k)
+        s_, t_, k_ = np.nonzero(idx_np[:, t0:t0 + n] >= 0)
+        t_ = t_ + t0
+        e_ = idx_np[s_, t_, k_]
+        d_, l_ = e_ // L, e_ % L
         lr = o_pk["layout_range"]
-        for j in pick[:64]:
-            s, t, k = int(s_[j]), int(t0 + t_[j]), int(k_[j])
-            e = int(idx[s, t, k])
-            d, l = divmod(e, L)
-            row = lr[d, l, s, 0] + sent["slot"][s, t, k]
-            codes, scales = orc.quantize_row(bits(xf[s * T + t]))
-            eq(pk["packed_x"][d, l, row], codes, f"packed_x ({s},{t},{k})")
-            eq(pk["packed_scales"][d, l, row], scales, f"packed_scales ({s},{t},{k})")
-            assert tuple(pk["packed_src_info"][d, l, row].tolist()) == (s, t)
+        row = lr[d_, l_, s_, 0] + sent["slot"][s_, t_, k_]
+        msg = (d_ * L + l_) * (R * cap) + row
+        tok = s_ * T + t_
+        _rows_equal(pk["packed_x"].view(-1, H), q[:, :H], tok, "packed_x (every message)", got_rows=msg)
+        _rows_equal(pk["packed_scales"].view(-1, H // 128), q[:, H:].view(torch.float32), tok,
+                    "packed_scales (every message)", got_rows=msg)
+        src_info = torch.from_numpy(np.stack([s_, t_], axis=1).astype(np.int32)).cuda()
+        _rows_equal(pk["packed_src_info"].view(-1, 2), src_info, np.arange(len(msg)),
+                    "packed_src_info (every message)", got_rows=msg)
         # sampled tokens of the microbatch: the oracle's k-ordered fp32 sum on a
         # one-rank sub-problem (one expert per k, one slot per token)
         toks = rng.choice(R * n, size=min(128, R * n), replace=False)
-        gs = [(int(q // n), int(t0 + q % n)) for q in toks]
+        gs = [(int(qq // n), int(t0 + qq % n)) for qq in toks]
         m = len(gs)
         sub_idx = np.full((1, m, K), -1, np.int64)
         sub_w = np.zeros((1, m, K), np.float32)
         sub_slot = np.full((1, m, K), -1, np.int32)
         y_sub = np.zeros((1, K, m, H), np.uint16)
+        y_sub_r = np.zeros((1, K, m, H), np.uint16)
+        yr_flat = y_rand.view(-1, H)
         for i, (s, t) in enumerate(gs):
             codes, scales = orc.quantize_row(bits(xf[s * T + t]))
             yrow = orc.ll_dequant(codes[None], scales[None])[0]
             for k in range(K):
-                if idx[s, t, k] >= 0:
+                e = int(idx_np[s, t, k])
+                if e >= 0:
                     sub_idx[0, i, k] = k
-                    sub_w[0, i, k] = w[s, t, k]
+                    sub_w[0, i, k] = w_np[s, t, k]
                     sub_slot[0, i, k] = i
                     y_sub[0, k, i] = yrow
+                    d, l = divmod(e, L)
+                    y_sub_r[0, k, i] = bits(yr_flat[(d * L + l) * R * cap + lr[d, l, s, 0] + sent["slot"][s, t, k]])
         sub_lr = np.zeros((1, K, 1, 2), np.int32)
         sub_lr[..., 1] = m
         exp = orc.ll_combine(y_sub, sub_idx, sub_w, sub_slot, sub_lr, 1, K, m)[0]
         got = np.stack([bits(out[s, t]) for s, t in gs])
         eq(got, exp, f"ll combine (sampled tokens, microbatch {t0})")
+        exp = orc.ll_combine(y_sub_r, sub_idx, sub_w, sub_slot, sub_lr, 1, K, m)[0]
+        got = np.stack([bits(out_y[s, t]) for s, t in gs])
+        eq(got, exp, f"ll combine of distinct expert rows (sampled tokens, microbatch {t0})")
 
 
 def test_decode_ll_full():
@@ -195,38 +249,41 @@ def test_skewed_ll_full_microbatches():
 
 
 def test_prefill_full_fp8_one_pass():
-    """The one-pass FP8 dispatches at the prefill size, in the bench's launch
-    configuration: every pair row equals the two-pass form (quantise, then the
-    fused FP8 dispatch) byte for byte, and sampled rows equal the oracle's
-    quantisation of their source token."""
+    """The FP8 dispatches at the prefill size, in the bench's launch
+    configuration: every row of the one-pass forms (into the permuted layout
+    and into the receive layout) and of the two-pass form (quantise, then the
+    fused FP8 dispatch) equals the oracle's quantisation of the source token
+    the oracle assigned to that row."""
     wl = inputs.WORKLOADS["prefill"]
     R, E, K, T, H, C = wl.R, wl.E, wl.K, wl.T, wl.H, wl.num_channels
     idx, w = inputs.make_routing(wl, 0)
     x = inputs.make_x(wl, 0, device="cuda")
+    xf = x.view(R * T, H)
     ctx = Context(R, E, K, T, H, num_channels=C)
     idxd, wd = idx.cuda(), w.cuda()
     h = ctx.notify_dispatch(idxd, ctx.get_dispatch_layout(idxd))
     n_def = H + H // 32
+    # the oracle's row assignment (positions do not depend on H: 8-channel stand-in)
+    o_lay = orc.layout(idx, R, E)
+    o_note = orc.notify(o_lay, R, E, T, C)
+    o_disp = orc.dispatch(np.zeros((R, T, 8), np.uint16), idx, w, o_note, R, E)
+    o_perm = orc.permute(idx, o_disp["recv_x"], o_note, R, E)
+    recv_tok = o_disp["recv_src_rank"].astype(np.int64) * T + o_disp["recv_src_idx"]
+    perm_tok = recv_tok[o_perm["perm_src_row"]]
+    q = _oracle_fp8_rows(xf)
     one = ctx.dispatch_permuted_quant(x, idxd, wd, h)
+    ctx.check()
+    _rows_equal(one["permuted_xq"][:, :n_def], q, perm_tok, "permuted_xq (one pass)")
+    eq(one["perm_src_token"], perm_tok.astype(np.int32), "perm_src_token (one pass)")
+    del one
     xq = ctx.quantize_fp8(x)
+    _rows_equal(xq[:, :n_def], q, np.arange(R * T), "quantised rows")
     two = ctx.dispatch_permuted_fp8(xq, idxd, wd, h)
     ctx.check()
-    assert torch.equal(one["permuted_xq"][:, :n_def], two["permuted_xq"][:, :n_def])
-    assert torch.equal(one["perm_src_token"], two["perm_src_token"])
-    assert torch.equal(one["perm_weight"], two["perm_weight"])
+    _rows_equal(two["permuted_xq"][:, :n_def], q, perm_tok, "permuted_xq (two passes)")
+    del two
     recv = ctx.dispatch_quant(x, idxd, wd, h)
-    recv2 = ctx.dispatch_fp8(xq, idxd, wd, h)
     ctx.check()
-    assert torch.equal(recv["recv_xq"][:, :n_def], recv2["recv_xq"][:, :n_def])
+    _rows_equal(recv["recv_xq"][:, :n_def], q, recv_tok, "recv_xq (one pass)")
     for k in ("recv_src_rank", "recv_src_idx", "recv_topk_idx", "recv_topk_weights"):
-        assert torch.equal(recv[k], recv2[k]), k
-    # sampled rows against the oracle's quantisation of their source token
-    rng = np.random.default_rng(3)
-    rows = rng.choice(one["permuted_xq"].shape[0], size=256, replace=False)
-    src = one["perm_src_token"].cpu().numpy()[rows]
-    xf = x.view(R * T, H)
-    got = bits(one["permuted_xq"][torch.from_numpy(rows).cuda()])
-    for i, g in enumerate(src):
-        codes, scales = orc.quantize_row(bits(xf[int(g)]))
-        eq(got[i, :H], codes, f"codes of row {rows[i]}")
-        eq(got[i, H:n_def].view(np.float32), scales, f"scales of row {rows[i]}")
+        eq(recv[k], o_disp[k], k)

@@ -96,6 +96,8 @@ def test_low_latency(R, E, K, T, H, cap, mbs, mask_p, seed):
     xd, idxd, wd = x.cuda(), idx.cuda(), w.cuda()
     out = torch.zeros(R, T, H, dtype=torch.bfloat16, device="cuda")
     o_out = np.zeros((R, T, H), np.uint16)
+    out_r = torch.zeros(R, T, H, dtype=torch.bfloat16, device="cuda")
+    o_out_r = np.zeros((R, T, H), np.uint16)
     for t0, n in mbs:
         pk = buf.send(xd, idxd, t0, n)
         counts = read_counts(buf, buf.current_buffer)
@@ -112,9 +114,15 @@ def test_low_latency(R, E, K, T, H, cap, mbs, mask_p, seed):
         yd = torch.from_numpy(y.view(np.int16)).view(torch.bfloat16).cuda()
         buf.combine(yd, idxd, wd, pk, t0, n, out=out)
         orc.ll_combine(y, idx, w, sent["slot"], o_pk["layout_range"], R, E, cap, t0, n, out=o_out)
+        # an expert output with a different row in every packed slot
+        L = E // R
+        yr = inputs.random_rows(R * L * R * cap, H, seed=seed * 17 + t0).view(R, L, R * cap, H)
+        buf.combine(yr.cuda(), idxd, wd, pk, t0, n, out=out_r)
+        orc.ll_combine(yr, idx, w, sent["slot"], o_pk["layout_range"], R, E, cap, t0, n, out=o_out_r)
     buf.check()
     torch.cuda.synchronize()
     eq(out, o_out, "ll combine")
+    eq(out_r, o_out_r, "ll combine of distinct expert rows")
 
 
 def test_low_latency_ping_pong_resets_counts():
@@ -189,31 +197,25 @@ def test_low_latency_layer_in_cuda_graph():
 
 
 def test_two_microbatches_on_two_streams():
-    """Dual-microbatch overlap: two low-latency buffers, each sending, receiving
-    and combining its own microbatch on its own stream at the same time, give
-    the results each gives alone (nothing waits across the streams)."""
+    """Dual-microbatch overlap ([P1] 高吞吐量模式, dual-batch overlap): two
+    low-latency buffers, each sending, receiving and combining its own
+    microbatch on its own stream at the same time (nothing waits across the
+    streams).  Each stream's packed rows, counts and combine output (of an
+    expert output with a distinct row per packed slot) equal the oracle's."""
     R, E, K, T, H, cap = 8, 64, 8, 96, 256, 96
+    L = E // R
     bufs = [LLBuffer(R, E, K, T, H, cap) for _ in range(2)]
-    ins = []
+    ins, ys = [], []
     for seed in (31, 32):
         idx = inputs.random_topk(R, E, K, T, seed, 0.05)
-        ins.append((inputs.random_x(R, T, H, seed).cuda(), idx.cuda(),
-                    inputs.random_weights(R, T, K, seed).cuda()))
-    # alone, one after the other
-    alone = []
-    for b, (x, idx, w) in zip(bufs, ins):
-        pk = b.dispatch(x, idx)
-        y = torch.randn(pk["packed_x"].shape, generator=torch.Generator(device="cuda").manual_seed(5),
-                        device="cuda").to(torch.bfloat16)
-        out = b.combine(y, idx, w, pk)
-        torch.cuda.synchronize()
-        b.check()
-        alone.append(({k: v.clone() for k, v in pk.items()}, y, out.clone()))
-    # together, on two streams
+        ins.append((inputs.random_x(R, T, H, seed), idx, inputs.random_weights(R, T, K, seed)))
+        ys.append(inputs.random_rows(R * L * R * cap, H, seed=seed).view(R, L, R * cap, H))
+    dev = [(x.cuda(), idx.cuda(), w.cuda(), y.cuda()) for (x, idx, w), y in zip(ins, ys)]
+    torch.cuda.synchronize()
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
     main = torch.cuda.current_stream()
     res = []
-    for st, b, (x, idx, w), (_, y, _) in zip(streams, bufs, ins, alone):
+    for st, b, (x, idx, w, y) in zip(streams, bufs, dev):
         st.wait_stream(main)
         with torch.cuda.stream(st):
             pk = b.dispatch(x, idx)
@@ -222,13 +224,10 @@ def test_two_microbatches_on_two_streams():
     for st in streams:
         main.wait_stream(st)
     torch.cuda.synchronize()
-    for b, (pk, out), (pk0, _, out0) in zip(bufs, res, alone):
+    for b, (pk, out), (x, idx, w), y in zip(bufs, res, ins, ys):
         b.check()
-        for k in ("packed_recv_count", "layout_range", "slot"):
-            eq(pk[k], bits(pk0[k]), k)
-        n = pk0["packed_recv_count"].cpu().numpy()
-        for d in range(R):
-            for l in range(E // R):
-                c = int(n[d, l])
-                eq(pk["packed_x"][d, l, :c], bits(pk0["packed_x"][d, l, :c]), "packed_x")
-        eq(out, bits(out0), "combine")
+        sent = orc.ll_send(x, idx, R, E, cap)
+        o_pk = orc.ll_pack(sent, R, E, H, cap)
+        check_ll_microbatch(pk, sent, o_pk, R, E, K, T, H, cap, 0, T, idx)
+        o_out = orc.ll_combine(y, idx, w, sent["slot"], o_pk["layout_range"], R, E, cap)
+        eq(out, o_out, "combine of the overlapped microbatch")
