@@ -10,8 +10,11 @@ The same run also times the low-latency layer on the decode workload
 as ``ll_decode``.  Further legs of the same line: ``fused_path`` (dispatch
 straight into the per-expert layout), ``expert_aligned`` (the permute into
 128-row aligned blocks), ``graph`` (the steps without a host wait, each one
-CUDA graph), ``fp8_rows`` (FP8 quantiser and FP8 dispatches) and ``e2e``
-(the step from pinned host buffers, copies inside the timed region).
+CUDA graph), ``fp8_rows`` (FP8 quantiser and FP8 dispatches), ``e2e``
+(the step from pinned host buffers, copies inside the timed region), and the
+other workloads timed the same way: ``skewed`` (the Zipf-skewed normal
+step), ``skewed_ll`` (its low-latency layer in 256-token microbatches) and
+``hier`` (the 4-node staged step).
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 a bounded sample of the same workload instead.
@@ -53,12 +56,14 @@ class L2Flush:
         self.r.max()
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes (read + write) per launch of the dominant kernel, from the ncu
-# capture named in "source" (a T=1024 case of the same kernel, scaled to a full
-# launch by the rows it moves); null for kernels not captured since they changed.
+# DRAM bytes (read + write) per launch of the dominant kernel: ncu's
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the same kernel
+# on a smaller case, scaled to a full launch by the rows it moves; only for a
+# kernel unchanged since that capture (else the roofline's traffic is null).
 TRAFFIC = {
     ("prefill", "permute"): {"bytes": 6.073e9,
-                             "source": "profiles/kernels_prefill_t1024_ncu_full.md (T=1024 capture x 4.024)"},
+                             "case": "one permute launch at T=1024 (R=8, E=256, K=8, H=7168), "
+                                     "scaled by the rows moved (x 4.024)"},
 }
 
 
@@ -208,7 +213,8 @@ def oracle_sample(workload, budget_s: float, min_s: float):
             break
     return {"value": tokens / t_total, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{tokens} tokens: {seed - 100} batches of R={w.R} x T={w.T} (E={w.E}, K={w.K}, H={w.H}), "
-                      f"single-threaded plain C oracle, {t_total:.1f} s"}
+                      f"single-threaded plain C oracle, {t_total:.1f} s",
+            "seconds": round(t_total, 3), "T": w.T}
 
 
 def _oracle_worker(args):
@@ -302,13 +308,18 @@ def run_reference(args, workload):
         r = oracle_sample(workload, budget_s=6.0, min_s=0.0)
         steps.append(r)
     value = statistics.median(s["value"] for s in steps)
+    sample_ms = statistics.median(s["seconds"] for s in steps) * 1e3
     cpu = dict(steps[-1])
     cpu["value"] = value
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup,
-        # one whole step of the workload at the sampled rate (each timed step is a bounded sample)
-        "ms_per_step": round(1e3 * workload.R * workload.T / value, 1) if value else None,
+        # each timed step is one bounded sample of the workload (T cut down):
+        # its own time, so that steps x ms_per_step is the time spent
+        "ms_per_step": round(sample_ms, 1),
+        "step": f"one sample of R={workload.R} x T={steps[-1]['T']} tokens of the {workload.name} workload",
+        # the whole workload's step at the sampled rate, for comparison with the GPU arm
+        "ms_per_full_step_extrapolated": round(1e3 * workload.R * workload.T / value, 1) if value else None,
         "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload.name, "R": workload.R, "E": workload.E, "K": workload.K,
@@ -323,6 +334,148 @@ def run_reference(args, workload):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+
+def kernel_entry(times_ms, nbytes, peak):
+    """Median / p10 / p90 of a kernel's event times; with its algorithmic
+    bytes, the effective GB/s and the fraction of the measured peak."""
+    med = statistics.median(times_ms)
+    e = {"us": round(med * 1e3, 2), "p10_us": round(pct(times_ms, 0.1) * 1e3, 2),
+         "p90_us": round(pct(times_ms, 0.9) * 1e3, 2)}
+    if nbytes is not None:
+        gbs = nbytes / (med * 1e-3) / 1e9
+        e.update({"algo_bytes": nbytes, "GBps": round(gbs, 1), "frac": round(gbs / peak, 3)})
+    return e
+
+
+def normal_leg(torch, w, seed, steps, warmup, flush):
+    """One more normal-mode workload timed like the main step (layout, notify
+    with its host wait, dispatch - staged for a hierarchical workload -,
+    permute, combine; identity expert; L2 flushed before every step): per
+    kernel times and fractions, the step time and tokens/s."""
+    from combine_get_dispatch_histograms_gb300 import Context, inputs
+    R, E, K, T, H, C = w.R, w.E, w.K, w.T, w.H, w.num_channels
+    hier = w.num_nodes > 1
+    topk_idx, topk_w = inputs.make_routing(w, seed)
+    x = inputs.make_x(w, seed, device="cuda")
+    idx_d, w_d = topk_idx.cuda(), topk_w.cuda()
+    ctx = Context(R, E, K, T, H, num_channels=C, num_nodes=w.num_nodes)
+    stream = torch.cuda.current_stream()
+    lay = ctx.get_dispatch_layout(idx_d, nodes=hier)
+    h = ctx.notify_dispatch(idx_d, lay)
+    recv = ctx.alloc_recv(h.num_recv_rows)
+    perm = dict(permuted_x=torch.empty(h.num_perm_rows, H, dtype=torch.bfloat16, device="cuda"),
+                perm_src_row=torch.empty(h.num_perm_rows, dtype=torch.int32, device="cuda"))
+    out = torch.empty(R, T, H, dtype=torch.bfloat16, device="cuda")
+    staging = None
+    if hier:
+        S = h.num_stage_rows
+        staging = dict(staging=torch.empty(S, H, dtype=torch.bfloat16, device="cuda"),
+                       stage_src_rank=torch.empty(S, dtype=torch.int32, device="cuda"),
+                       stage_src_idx=torch.empty(S, dtype=torch.int32, device="cuda"))
+
+    def step(ev):
+        ev[0].record(stream)
+        ctx.get_dispatch_layout(idx_d, nodes=hier, out=lay)
+        ev[1].record(stream)
+        ctx.notify_dispatch(idx_d, lay, handle=h)
+        ev[2].record(stream)
+        if hier:
+            ctx.dispatch_hier(x, idx_d, w_d, h, out=recv, staging=staging)
+        else:
+            ctx.dispatch(x, idx_d, w_d, h, out=recv)
+        ev[3].record(stream)
+        ctx.permute(h, recv, out=perm)
+        ev[4].record(stream)
+        ctx.combine(h, perm["permuted_x"], idx_d, w_d, out=out, hier=hier)
+        ev[5].record(stream)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(warmup + steps)]
+    for i in range(warmup + steps):
+        flush()
+        step(evs[i])
+    torch.cuda.synchronize()
+    ctx.check()
+    evs = evs[warmup:]
+    names = ["layout", "notify", "dispatch", "permute", "combine"]
+    tokens, copies, pairs = R * T, h.num_recv_rows, h.num_perm_rows
+    ab = algo_bytes(H, K, tokens, copies, pairs, h.num_stage_rows if hier else 0)
+    peak, _ = measured_hbm_gbs()
+    kernels = {n: kernel_entry([e[j].elapsed_time(e[j + 1]) for e in evs], ab.get(n), peak)
+               for j, n in enumerate(names)}
+    ms = sum(e[0].elapsed_time(e[5]) for e in evs) / len(evs)
+    res = {"workload": w.name, "R": R, "E": E, "K": K, "T": T, "H": H, "num_nodes": w.num_nodes,
+           "router": w.router, "copies": copies, "pairs": pairs, "ms_per_step": round(ms, 4),
+           "tokens_per_s": round(tokens / (ms / 1e3), 1), "kernels": kernels,
+           "effective_GBps": round(sum(ab.values()) / (sum(statistics.median(
+               e[j].elapsed_time(e[j + 1]) for e in evs) for j in (2, 3, 4)) * 1e-3) / 1e9, 1)}
+    if hier:
+        res["staged_rows"] = h.num_stage_rows
+        res["dispatch_note"] = "stage A (one row per destination node) + stage B (forward inside the node)"
+    return res
+
+
+def ll_microbatch_leg(torch, w, seed, steps, warmup, flush):
+    """The low-latency layer of a workload whose T exceeds the per-region cap:
+    T split into microbatches of <= cap tokens, each sent, received and
+    combined (expert output: a distinct row per packed slot); per kernel the
+    median over every microbatch of every timed step, and the whole batch's
+    time."""
+    from combine_get_dispatch_histograms_gb300 import LLBuffer, inputs
+    R, E, K, T, H, cap = w.R, w.E, w.K, w.T, w.H, w.ll_cap
+    L = E // R
+    topk_idx, topk_w = inputs.make_routing(w, seed)
+    x = inputs.make_x(w, seed, device="cuda")
+    idx_d, w_d = topk_idx.cuda(), topk_w.cuda()
+    buf = LLBuffer(R, E, K, T, H, cap)
+    pk = buf.alloc_packed()
+    y = inputs.random_rows(R * L * R * cap, H, seed, device="cuda").view(R, L, R * cap, H)
+    out = torch.empty(R, T, H, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    mbs = [(t0, min(cap, T - t0)) for t0 in range(0, T, cap)]
+    names = ["ll_send", "ll_recv", "ll_combine"]
+    per = {n: [] for n in names}
+    batch_ms = []
+    peak, _ = measured_hbm_gbs()
+    nbytes = {n: [] for n in names}
+    idx_np = topk_idx.numpy()
+    for i in range(warmup + steps):
+        tot = 0.0
+        for t0, n in mbs:
+            flush()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record(stream)
+            buf.send(x, idx_d, t0, n, out=pk)
+            e[1].record(stream)
+            buf.recv(pk)
+            e[2].record(stream)
+            buf.combine(y, idx_d, w_d, pk, t0, n, out=out)
+            e[3].record(stream)
+            torch.cuda.synchronize()
+            if i >= warmup:
+                for j, nm in enumerate(names):
+                    per[nm].append(e[j].elapsed_time(e[j + 1]))
+                tot += e[0].elapsed_time(e[3])
+                if i == warmup:
+                    b = ll_algo_bytes(H, R * n, int((idx_np[:, t0:t0 + n] >= 0).sum()))
+                    for nm in names:
+                        nbytes[nm].append(b[nm])
+        if i >= warmup:
+            batch_ms.append(tot)
+    buf.check()
+    kernels = {}
+    for nm in names:
+        med = statistics.median(per[nm])
+        mb = statistics.median(nbytes[nm])
+        kernels[nm] = kernel_entry(per[nm], mb, peak)
+        kernels[nm]["algo_bytes_note"] = "median over the microbatches"
+    return {"workload": w.name, "R": R, "E": E, "K": K, "T": T, "H": H, "cap": cap, "microbatches": len(mbs),
+            "us_per_microbatch": round(statistics.median(per["ll_send"]) * 1e3 + statistics.median(
+                per["ll_recv"]) * 1e3 + statistics.median(per["ll_combine"]) * 1e3, 2),
+            "ms_per_batch": round(statistics.median(batch_ms), 4),
+            "tokens_per_s": round(R * T / (statistics.median(batch_ms) / 1e3), 1),
+            "kernels": kernels,
+            "timing": "per-kernel events on one stream, L2 flushed before every microbatch"}
+
 
 def main():
     ap = argparse.ArgumentParser()
@@ -342,6 +495,8 @@ def main():
                     help="with --ll-only: E of the decode layer (fewer experts: same messages, smaller buffers)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="skip the skewed and hierarchical legs of the default prefill run")
     args = ap.parse_args()
 
     from combine_get_dispatch_histograms_gb300 import inputs
@@ -842,6 +997,20 @@ def main():
               "l2": L2_DESC}
         del y_ll, pk, buf
 
+    # ---- the other workloads: skewed (normal + LL microbatches) and hierarchical ----
+    extra = {}
+    if w.name == "prefill" and not args.tokens and not args.no_extra_workloads:
+        ksteps, kwarm = min(args.steps, 10), max(3, min(args.warmup, 5))
+        for name, fn, wl in (("skewed", normal_leg, inputs.WORKLOADS["skewed"]),
+                             ("skewed_ll", ll_microbatch_leg, inputs.WORKLOADS["skewed"]),
+                             ("hier", normal_leg, inputs.WORKLOADS["hier"])):
+            try:
+                extra[name] = fn(torch, wl, seed + 3, ksteps, kwarm, flush)
+                extra[name]["steps"], extra[name]["warmup"] = ksteps, kwarm
+            except Exception as exc:  # reported, not hidden
+                extra[name] = f"failed: {exc}"
+            torch.cuda.empty_cache()
+
     clocks = sampler.stop()
 
     # ---- end to end through the public API with host buffers ------------------------
@@ -1023,7 +1192,7 @@ def main():
                 "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "algo_bytes_per_launch": ab[dom], "traffic": tr["bytes"] if tr else None,
-                "traffic_source": tr["source"] if tr else None}
+                "traffic_case": tr["case"] if tr else None}
 
     cpu = None
     if not args.no_cpu and world == 1:  # the CPU baseline is timed at N=1 only
@@ -1055,6 +1224,9 @@ def main():
         "expert_aligned": aligned,
         "graph": nw_graph,
         "fp8_rows": fp8,
+        "skewed": extra.get("skewed"),
+        "skewed_ll": extra.get("skewed_ll"),
+        "hier": extra.get("hier"),
     }
     print(json.dumps(add_nominal_pct(line)), flush=True)
     epdist.shutdown()
