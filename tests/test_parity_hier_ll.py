@@ -231,3 +231,28 @@ def test_two_microbatches_on_two_streams():
         check_ll_microbatch(pk, sent, o_pk, R, E, K, T, H, cap, 0, T, idx)
         o_out = orc.ll_combine(y, idx, w, sent["slot"], o_pk["layout_range"], R, E, cap)
         eq(out, o_out, "combine of the overlapped microbatch")
+
+
+def test_low_latency_x_only_16_byte_aligned():
+    """x may be only 16-byte aligned (the documented requirement): the send
+    then loads each lane's channels with two 16-byte loads instead of one
+    32-byte load; the messages and the combine equal the oracle's."""
+    R, E, K, T, H, cap = 8, 64, 8, 20, 1024, 20
+    idx = inputs.random_topk(R, E, K, T, 41, 0.1)
+    x = inputs.random_x(R, T, H, 41)
+    w = inputs.random_weights(R, T, K, 41)
+    big = torch.empty(R * T * H + 8, dtype=torch.bfloat16, device="cuda")
+    xd = big[8:].view(R, T, H)          # 16 bytes past a 32-byte boundary
+    assert xd.data_ptr() % 32 == 16
+    xd.copy_(x.cuda())
+    buf = LLBuffer(R, E, K, T, H, cap)
+    pk = buf.dispatch(xd, idx.cuda())
+    L = E // R
+    yr = inputs.random_rows(R * L * R * cap, H, seed=41).view(R, L, R * cap, H)
+    out = buf.combine(yr.cuda(), idx.cuda(), w.cuda(), pk)
+    torch.cuda.synchronize()
+    buf.check()
+    sent = orc.ll_send(x, idx, R, E, cap)
+    o_pk = orc.ll_pack(sent, R, E, H, cap)
+    check_ll_microbatch(pk, sent, o_pk, R, E, K, T, H, cap, 0, T, idx)
+    eq(out, orc.ll_combine(yr, idx, w, sent["slot"], o_pk["layout_range"], R, E, cap), "ll combine")
