@@ -468,7 +468,13 @@ def ll_microbatch_leg(torch, w, seed, steps, warmup, flush):
         mb = statistics.median(nbytes[nm])
         kernels[nm] = kernel_entry(per[nm], mb, peak)
         kernels[nm]["algo_bytes_note"] = "median over the microbatches"
+    batch_bytes = sum(sum(nbytes[nm]) for nm in names)
+    bm = statistics.median(batch_ms)
     return {"workload": w.name, "R": R, "E": E, "K": K, "T": T, "H": H, "cap": cap, "microbatches": len(mbs),
+            "batch": {"algo_bytes": batch_bytes, "GBps": round(batch_bytes / (bm * 1e-3) / 1e9, 1),
+                      "frac": round(batch_bytes / (bm * 1e-3) / 1e9 / peak, 3),
+                      "what": "all microbatches' send, receive and combine bytes over the batch time "
+                              "(per-kernel events, L2 flushed before each microbatch)"},
             "us_per_microbatch": round(statistics.median(per["ll_send"]) * 1e3 + statistics.median(
                 per["ll_recv"]) * 1e3 + statistics.median(per["ll_combine"]) * 1e3, 2),
             "ms_per_batch": round(statistics.median(batch_ms), 4),
@@ -985,8 +991,13 @@ def main():
         d_pairs = int((d_idx >= 0).sum())
         lbytes = ll_algo_bytes(dw.H, dw.R * dw.T, d_pairs)
         peak, _ = measured_hbm_gbs()
+        layer_bytes = sum(lbytes.values())
         ll = {"workload": "decode", "R": dw.R, "T": dw.T, "H": dw.H, "cap": dw.ll_cap,
               "us_per_layer": round(layer_us, 2),
+              # the layer as one unit: per-kernel fractions move bytes between
+              # kernels (a kernel's dirty lines are written back during the next)
+              "layer": {"algo_bytes": layer_bytes, "GBps": round(layer_bytes / (layer_us * 1e-6) / 1e9, 1),
+                        "frac": round(layer_bytes / (layer_us * 1e-6) / 1e9 / peak, 3)},
               "us_per_layer_with_kernel_events": round(layer_instrumented_us, 2),
               "us_per_layer_cuda_graph": graph_us,
               "dual_microbatch_overlap": dual,

@@ -80,7 +80,11 @@ def test_low_latency_random_config(seed):
     xd, idxd, wd = x.cuda(), idx.cuda(), w.cuda()
     out = torch.zeros(R, T, H, dtype=torch.bfloat16, device="cuda")
     o_out = np.zeros((R, T, H), np.uint16)
+    out_r = torch.zeros(R, T, H, dtype=torch.bfloat16, device="cuda")
+    o_out_r = np.zeros((R, T, H), np.uint16)
     L = E // R
+    yr = inputs.random_rows(R * L * R * cap, H, seed=seed).view(R, L, R * cap, H)
+    yrd = yr.cuda()
     for t0 in range(0, T, cap):
         n = min(cap, T - t0)
         pk = buf.dispatch(xd, idxd, t0, n)
@@ -98,8 +102,11 @@ def test_low_latency_random_config(seed):
         y = orc.ll_dequant(o_pk["packed_x"], o_pk["packed_scales"])
         buf.combine(torch.from_numpy(y.view(np.int16)).view(torch.bfloat16).cuda(), idxd, wd, pk, t0, n, out=out)
         orc.ll_combine(y, idx, w, sent["slot"], o_pk["layout_range"], R, E, cap, t0, n, out=o_out)
+        buf.combine(yrd, idxd, wd, pk, t0, n, out=out_r)
+        orc.ll_combine(yr, idx, w, sent["slot"], o_pk["layout_range"], R, E, cap, t0, n, out=o_out_r)
     buf.check()
     eq(out, o_out, "ll combine")
+    eq(out_r, o_out_r, "ll combine of distinct expert rows")
 
 
 def _wide_range_x(R, T, H, seed):

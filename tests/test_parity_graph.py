@@ -22,7 +22,10 @@ def _alloc(ctx: Context, hier: bool):
              perm=dict(permuted_x=torch.empty(pmax, ctx.H, dtype=torch.bfloat16, device="cuda"),
                        perm_src_row=torch.empty(pmax, dtype=torch.int32, device="cuda")),
              out=torch.empty(ctx.R, ctx.T, ctx.H, dtype=torch.bfloat16, device="cuda"),
-             h=ctx.alloc_handle())
+             h=ctx.alloc_handle(),
+             # an expert output with a distinct row per permuted row, combined too
+             y=inputs.random_rows(pmax, ctx.H, seed=pmax).cuda(),
+             out_y=torch.empty(ctx.R, ctx.T, ctx.H, dtype=torch.bfloat16, device="cuda"))
     if hier:
         b["staging"] = dict(staging=torch.empty(smax, ctx.H, dtype=torch.bfloat16, device="cuda"),
                             stage_src_rank=torch.empty(smax, dtype=torch.int32, device="cuda"),
@@ -40,6 +43,7 @@ def _step(ctx: Context, x, idx, w, b, hier: bool):
         ctx.dispatch(x, idx, w, h, out=b["recv"])
     ctx.permute(h, b["recv"], out=b["perm"])
     ctx.combine(h, b["perm"]["permuted_x"], idx, w, out=b["out"], hier=hier)
+    ctx.combine(h, b["y"], idx, w, out=b["out_y"], hier=hier)
 
 
 def _compare(ctx: Context, b, x, idx, w, hier: bool):
@@ -75,6 +79,12 @@ def _compare(ctx: Context, b, x, idx, w, hier: bool):
     else:
         o_out = orc.combine(o_perm["permuted_x"], o_perm["perm_pos"], idx, w, R, E, "ord32")
     eq(b["out"], o_out, "combine (fp32 order)")
+    y = b["y"][:npm].cpu()
+    if hier:
+        o_y = orc.combine_hier(y, o_perm["perm_pos"], idx, w, R, E, N)
+    else:
+        o_y = orc.combine(y, o_perm["perm_pos"], idx, w, R, E, "ord32")
+    eq(b["out_y"], o_y, "combine of distinct expert rows")
 
 
 CASES = [
