@@ -369,7 +369,7 @@ struct EngineLaunch {
     size_t smem;
 };
 
-static EngineLaunch plan_engine(const ep_ctx* c, int64_t n_units, int64_t row_bytes, int fanout) {
+static EngineLaunch plan_engine(const ep_ctx* c, int64_t n_units, int64_t row_bytes, int fanout, CopyKind kind) {
     EngineLaunch p;
     p.g.n_units = n_units;
     p.g.n_units_dev = nullptr;
@@ -379,7 +379,7 @@ static EngineLaunch plan_engine(const ep_ctx* c, int64_t n_units, int64_t row_by
     p.g.status = c->status;
     p.depth = c->copy_read_depth;
     // copy_ctas_per_sm persistent CTAs per SM, each with copy_stage_bytes of staging
-    const size_t budget = (size_t)c->copy_stage_bytes;
+    const size_t budget = (size_t)c->copy_stage_bytes[kind];
     const size_t fixed = engine_stage_offset(fanout);
     const size_t stage_room = budget > fixed ? budget - fixed : 16 * 1024;
     int64_t chunk = row_bytes;
@@ -392,7 +392,7 @@ static EngineLaunch plan_engine(const ep_ctx* c, int64_t n_units, int64_t row_by
     if (stages < p.depth + 1) stages = p.depth + 1;
     p.g.stages = stages;
     p.smem = fixed + (size_t)stages * chunk;
-    const int64_t max_grid = (int64_t)c->num_sms * c->copy_ctas_per_sm;
+    const int64_t max_grid = (int64_t)c->num_sms * c->copy_ctas_per_sm[kind];
     const int64_t want = (n_units + 7) / 8;  // at least 8 units per CTA
     p.grid = (int)(want < max_grid ? (want < 1 ? 1 : want) : max_grid);
     return p;
@@ -469,7 +469,7 @@ ep_status dispatch_rows(ep_ctx* c, const void* x, int64_t row_bytes, const int64
     r.row_bytes = row_bytes;
     r.recv_rows = recv_capacity_rows;
     r.status = c->status;
-    EngineLaunch p = plan_engine(c, (int64_t)f.num_ranks * f.num_tokens, r.row_bytes, f.num_ranks);
+    EngineLaunch p = plan_engine(c, (int64_t)f.num_ranks * f.num_tokens, r.row_bytes, f.num_ranks, COPY_SCATTER);
     st = launch_engine(c, r, p, as_stream(stream), "dispatch scatter");
     if (st == EP_OK) c->last_launches = 1;
     return st;
@@ -505,7 +505,7 @@ ep_status permute_rows(ep_ctx* c, const ep_dispatch_handle* h, const void* recv_
     r.row_bytes = row_bytes;
     r.perm_rows = perm_capacity_rows;
     r.status = c->status;
-    EngineLaunch p = plan_engine(c, num_recv_rows, r.row_bytes, f.num_topk);
+    EngineLaunch p = plan_engine(c, num_recv_rows, r.row_bytes, f.num_topk, COPY_PERMUTE);
     p.g.n_units_dev = h->rank_base + f.num_ranks;  // rows actually received, at most num_recv_rows
     st = launch_engine(c, r, p, as_stream(stream), "local permute");
     if (st == EP_OK) c->last_launches = 1;
@@ -540,7 +540,7 @@ ep_status dispatch_permuted_rows(ep_ctx* c, const void* x, int64_t row_bytes, co
     r.row_bytes = row_bytes;
     r.perm_rows = perm_capacity_rows;
     r.status = c->status;
-    EngineLaunch p = plan_engine(c, (int64_t)f.num_ranks * f.num_tokens, r.row_bytes, f.num_topk);
+    EngineLaunch p = plan_engine(c, (int64_t)f.num_ranks * f.num_tokens, r.row_bytes, f.num_topk, COPY_FUSED);
     st = launch_engine(c, r, p, as_stream(stream), "fused dispatch");
     if (st == EP_OK) c->last_launches = 1;
     return st;
@@ -610,7 +610,7 @@ extern "C" ep_status ep_dispatch_hier(ep_ctx* c, const void* x, const int64_t* t
     a.row_bytes = row_bytes;
     a.stage_rows = stage_capacity_rows;
     a.status = c->status;
-    EngineLaunch pa = plan_engine(c, (int64_t)f.num_ranks * f.num_tokens, row_bytes, f.num_nodes);
+    EngineLaunch pa = plan_engine(c, (int64_t)f.num_ranks * f.num_tokens, row_bytes, f.num_nodes, COPY_STAGE);
     st = launch_engine(c, a, pa, as_stream(stream), "hierarchical stage A");
     if (st != EP_OK) return st;
     StageBRoute b;
@@ -635,7 +635,7 @@ extern "C" ep_status ep_dispatch_hier(ep_ctx* c, const void* x, const int64_t* t
     b.row_bytes = row_bytes;
     b.recv_rows = recv_capacity_rows;
     b.status = c->status;
-    EngineLaunch pb = plan_engine(c, c->totals_known ? c->last_total_stage : stage_capacity_rows, row_bytes, c->G);
+    EngineLaunch pb = plan_engine(c, c->totals_known ? c->last_total_stage : stage_capacity_rows, row_bytes, c->G, COPY_STAGE);
     pb.g.n_units_dev = h->stage_base + f.num_ranks;  // rows actually staged
     st = launch_engine(c, b, pb, as_stream(stream), "hierarchical stage B");
     if (st == EP_OK) c->last_launches = 2;

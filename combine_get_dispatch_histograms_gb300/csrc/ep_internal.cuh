@@ -96,9 +96,9 @@ struct ep_ctx {
     int32_t* host_block_dev;
     cudaEvent_t ev_counts;
     int64_t wait_timeout_ns;
-    // copy-engine launch shape (defaults; EP_COPY_CTAS_PER_SM, EP_COPY_STAGE_KB and
-    // EP_COPY_READ_DEPTH override them at context creation)
-    int copy_ctas_per_sm, copy_stage_bytes, copy_read_depth;
+    // copy-engine launch shape per route kind (ep::CopyKind), chosen at context
+    // creation; environment variables override them for sweeps
+    int copy_ctas_per_sm[4], copy_stage_bytes[4], copy_read_depth;
     // totals of the last notify (host copies), sizes of later launches
     int64_t last_total_recv, last_total_perm, last_total_stage;
     bool totals_known;  // false after a notify that did not wait for the counts
@@ -107,6 +107,9 @@ struct ep_ctx {
 };
 
 namespace ep {
+
+// route kinds of the copy engine, each with its own launch shape
+enum CopyKind : int { COPY_PERMUTE = 0, COPY_SCATTER = 1, COPY_FUSED = 2, COPY_STAGE = 3 };
 
 // ---- small device helpers -------------------------------------------------------
 __device__ __forceinline__ void flag(uint32_t* status, uint32_t bits) { atomicOr(status, bits); }

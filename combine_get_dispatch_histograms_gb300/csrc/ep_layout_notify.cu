@@ -610,8 +610,25 @@ extern "C" ep_status ep_ctx_create(const ep_config* cfg, ep_ctx** out) {
     c->G = cfg->num_ranks / cfg->num_nodes;
     c->tiles = make_tiles(cfg->num_tokens, cfg->num_channels);
     c->wait_timeout_ns = 2000000000ll;
-    c->copy_ctas_per_sm = env_int("EP_COPY_CTAS_PER_SM", 2, 1, 8);
-    c->copy_stage_bytes = env_int("EP_COPY_STAGE_KB", 64, 16, 220) * 1024;
+    {
+        // launch shape per copy route kind (measured on GB300): two CTAs per SM
+        // with 64 KB of staging each, except the dispatch scatter, whose row
+        // fans out to every destination rank: one CTA per SM with 160 KB
+        // (skewed 803 -> 757 us, prefill unchanged; the permute and the
+        // staging kernels are slower that way).  EP_COPY_CTAS_PER_SM and
+        // EP_COPY_STAGE_KB set every kind, EP_<KIND>_CTAS_PER_SM and
+        // EP_<KIND>_STAGE_KB one kind (PERMUTE, SCATTER, FUSED, STAGE).
+        static const char* const kinds[4] = {"PERMUTE", "SCATTER", "FUSED", "STAGE"};
+        static const int dflt_ctas[4] = {2, 1, 2, 2};
+        static const int dflt_kb[4] = {64, 160, 64, 64};
+        for (int k = 0; k < 4; ++k) {
+            char n1[48], n2[48];
+            snprintf(n1, sizeof n1, "EP_%s_CTAS_PER_SM", kinds[k]);
+            snprintf(n2, sizeof n2, "EP_%s_STAGE_KB", kinds[k]);
+            c->copy_ctas_per_sm[k] = env_int(n1, env_int("EP_COPY_CTAS_PER_SM", dflt_ctas[k], 1, 8), 1, 8);
+            c->copy_stage_bytes[k] = env_int(n2, env_int("EP_COPY_STAGE_KB", dflt_kb[k], 16, 220), 16, 220) * 1024;
+        }
+    }
     c->copy_read_depth = env_int("EP_COPY_READ_DEPTH", 2, 1, 3);
     cudaError_t e = cudaGetDevice(&c->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
