@@ -99,6 +99,7 @@ struct ep_ctx {
     // copy-engine launch shape per route kind (ep::CopyKind), chosen at context
     // creation; environment variables override them for sweeps
     int copy_ctas_per_sm[4], copy_stage_bytes[4], copy_read_depth;
+    bool copy_shape_forced[4];  // set from the environment: used as given
     // totals of the last notify (host copies), sizes of later launches
     int64_t last_total_recv, last_total_perm, last_total_stage;
     bool totals_known;  // false after a notify that did not wait for the counts

@@ -627,6 +627,8 @@ extern "C" ep_status ep_ctx_create(const ep_config* cfg, ep_ctx** out) {
             snprintf(n2, sizeof n2, "EP_%s_STAGE_KB", kinds[k]);
             c->copy_ctas_per_sm[k] = env_int(n1, env_int("EP_COPY_CTAS_PER_SM", dflt_ctas[k], 1, 8), 1, 8);
             c->copy_stage_bytes[k] = env_int(n2, env_int("EP_COPY_STAGE_KB", dflt_kb[k], 16, 220), 16, 220) * 1024;
+            c->copy_shape_forced[k] = getenv(n1) || getenv(n2) || getenv("EP_COPY_CTAS_PER_SM") ||
+                                      getenv("EP_COPY_STAGE_KB");
         }
     }
     c->copy_read_depth = env_int("EP_COPY_READ_DEPTH", 2, 1, 3);
