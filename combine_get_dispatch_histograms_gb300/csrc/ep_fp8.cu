@@ -8,6 +8,8 @@
 // padded to 16 bytes -- with the same codec as the low-latency send, and the
 // scatter / permute / fused-dispatch row movers carry those rows instead of the
 // 2H-byte bf16 rows.
+#include <cstdlib>
+
 #include "ep_fp8.cuh"
 
 namespace ep {
@@ -325,9 +327,20 @@ extern "C" ep_status ep_dispatch_permuted_fp8(ep_ctx* c, const uint8_t* xq, cons
 
 template <bool kRecv>
 static ep_status launch_quant_scatter(ep_ctx* c, const QuantScatterArgs& a, void* stream) {
-    // three CTAs per SM, ~72 KB each: two FP8 row buffers and as many staged x rows as fit
+    // three CTAs per SM, ~72 KB each: two FP8 row buffers and as many staged x
+    // rows as fit (EP_QS_CTAS_PER_SM and EP_QS_STAGE_KB override the shape)
+    static const int qs_ctas = [] {
+        const char* v = getenv("EP_QS_CTAS_PER_SM");
+        const int x = v ? atoi(v) : 3;
+        return x < 1 ? 1 : (x > 8 ? 8 : x);
+    }();
+    static const int qs_kb = [] {
+        const char* v = getenv("EP_QS_STAGE_KB");
+        const int x = v ? atoi(v) : 72;
+        return x < 32 ? 32 : (x > 220 ? 220 : x);
+    }();
     const int64_t row_bytes = (int64_t)a.H * 2;
-    const size_t budget = 72 * 1024;
+    const size_t budget = (size_t)qs_kb * 1024;
     int stages = (int)((budget - qs_fixed_smem() - 2 * (size_t)a.row_q) / (size_t)row_bytes);
     if (stages > kQsMaxStages) stages = kQsMaxStages;
     if (stages < 2) stages = 2;
@@ -338,7 +351,7 @@ static ep_status launch_quant_scatter(ep_ctx* c, const QuantScatterArgs& a, void
                                      (int)smem));
         if (c->device >= 0 && c->device < kMaxDevicesTracked) raised[c->device] = (int)smem;
     }
-    int64_t grid = (int64_t)c->num_sms * 3;
+    int64_t grid = (int64_t)c->num_sms * qs_ctas;
     if (grid > a.tokens) grid = a.tokens;
     quant_scatter_kernel<kRecv><<<(int)grid, 256, smem, as_stream(stream)>>>(a, stages, c->wait_timeout_ns);
     EP_CHECK_LAUNCH("quant_scatter_kernel");
