@@ -464,9 +464,7 @@ def ll_microbatch_leg(torch, w, seed, steps, warmup, flush):
     buf.check()
     kernels = {}
     for nm in names:
-        med = statistics.median(per[nm])
-        mb = statistics.median(nbytes[nm])
-        kernels[nm] = kernel_entry(per[nm], mb, peak)
+        kernels[nm] = kernel_entry(per[nm], statistics.median(nbytes[nm]), peak)
         kernels[nm]["algo_bytes_note"] = "median over the microbatches"
     batch_bytes = sum(sum(nbytes[nm]) for nm in names)
     bm = statistics.median(batch_ms)
