@@ -118,3 +118,26 @@ def test_noalloc_rejects_oversized_problems():
                                             None, None)
     assert rc == -3
     assert b"scratch" in lib.ep_last_error()
+
+
+def test_noalloc_scratch_boundary():
+    """The largest problem the fixed scratch holds runs and matches the
+    oracle; one more tile is rejected with EP_ERR_CAPACITY.  R=8, E=256, no
+    node outputs: the scratch needs 4 * (128 + 8 * ceil(T / 256) * 264) bytes,
+    at most 1 MiB up to T = 124 * 256."""
+    lib = _lib.load()
+    R, E, K = 8, 256, 8
+    T = 124 * 256
+    assert 4 * (128 + R * (T // 256) * (E + R)) <= 1 << 20 < 4 * (128 + R * (T // 256 + 1) * (E + R))
+    idx = inputs.random_topk(R, E, K, T, 9, 0.01)
+    exp = orc.layout(idx, R, E)
+    got, status = _noalloc(lib, R, E, K, T, 1, idx.cuda(), False)
+    assert status == 0
+    for k in KEYS:
+        eq(got[k], exp[k], k)
+    T2 = T + 1
+    dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
+    idx2 = torch.zeros(1, dtype=torch.int64, device="cuda")
+    rc = lib.ep_get_dispatch_layout_noalloc(R, E, K, T2, 1, _p(idx2), _p(dummy), _p(dummy), _p(dummy), None, None,
+                                            None, None)
+    assert rc == -3
