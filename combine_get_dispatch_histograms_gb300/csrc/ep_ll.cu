@@ -351,8 +351,8 @@ __global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(LLRecvArgs a) {
         const int64_t p = ((int64_t)d * L + l) * rows_per_expert + begin + i;
         const int4* src = reinterpret_cast<const int4*>(msg + 16);
         int4* dx = reinterpret_cast<int4*>(a.packed_x + p * H);
-        // every load of the message (up to 16 vectors per lane) before the
-        // stores that consume them; the scales ride along
+        // the message's vectors in batches of eight per lane, each batch's
+        // loads before its stores; the scales ride along
         const float* sc = reinterpret_cast<const float*>(msg + 16 + H);
         float scv = lane < S ? __ldcg(sc + lane) : 0.0f;
         for (int v0 = 0; v0 < nv; v0 += 8 * 32) {
