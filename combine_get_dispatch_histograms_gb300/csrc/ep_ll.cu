@@ -539,7 +539,18 @@ extern "C" ep_status ep_ll_send(ep_ll_buffer* b, const void* x, const int64_t* t
     // count stores after every data store of the send grid
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(a.R);
-    lc.blockDim = dim3(256);
+    // 128 threads: four warps of 32 registers fit in the registers the send's
+    // three CTAs per SM leave free, so the publisher's histogram runs beside
+    // the send instead of after it (eager decode layer 111.0 -> 109.8 us,
+    // skewed send 65.5 -> 63.5 us per microbatch; two microbatches overlapped
+    // on two streams 105.5 -> 107.5 us per layer).  EP_LL_PUB_THREADS (32..256)
+    // overrides it.
+    static const int pub_threads = [] {
+        const char* v = getenv("EP_LL_PUB_THREADS");
+        const int x = v ? atoi(v) / 32 * 32 : 128;
+        return x < 32 ? 32 : (x > 256 ? 256 : x);
+    }();
+    lc.blockDim = dim3(pub_threads);
     lc.dynamicSmemBytes = sizeof(int32_t) * (size_t)a.E;
     lc.stream = s;
     cudaLaunchAttribute attr[1];
