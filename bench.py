@@ -846,6 +846,26 @@ def main():
         buf.check()
         lname = ["ll_send", "ll_recv", "ll_combine"]
         lper = {n: statistics.median(e[j].elapsed_time(e[j + 1]) for e in lev) for j, n in enumerate(lname)}
+        # each kernel alone: L2 flushed (and its dirty lines written back)
+        # right before it, so that no kernel pays for the previous one's
+        # write-backs nor gains from its lines still in L2
+        iso = {n: [] for n in lname}
+        for i in range(args.warmup + args.steps):
+            for j, n in enumerate(lname):
+                flush()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                if j == 0:
+                    buf.send(d_x, d_idx_d, out=pk)
+                elif j == 1:
+                    buf.recv(pk)
+                else:
+                    buf.combine(y_ll, d_idx_d, d_w_d, pk, out=d_out)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if i >= args.warmup:
+                    iso[n].append(e0.elapsed_time(e1))
+        buf.check()
         layer_instrumented_us = statistics.median(e[0].elapsed_time(e[3]) for e in lev) * 1e3
         # the layer alone, events only at its ends: the per-kernel events above
         # sit between the programmatic-dependent launches and serialise them
@@ -1003,6 +1023,9 @@ def main():
               "kernels": {n: {"us": round(lper[n] * 1e3, 2), "algo_bytes": lbytes[n],
                               "GBps": round(lbytes[n] / (lper[n] * 1e-3) / 1e9, 1),
                               "frac": round(lbytes[n] / (lper[n] * 1e-3) / 1e9 / peak, 3)} for n in lname},
+              "kernels_isolated": {n: kernel_entry(iso[n], lbytes[n], peak) for n in lname},
+              "kernels_isolated_how": "each kernel with L2 flushed and written back right before it "
+                                      "(the chained figures above are the layer's own)",
               "l2": L2_DESC}
         del y_ll, pk, buf
 
