@@ -128,3 +128,21 @@ def run_gpu_ll(R, E, K, T, H, cap, x, idx, microbatches):
         outs.append({k: v.clone() for k, v in pk.items()})
     buf.check()
     return buf, outs
+
+
+def check_ll_microbatch_equal(pk, sent, o_pk, R, E, T, cap, t0=0, n=None):
+    """The low-latency send's slots and the receive's packed outputs against
+    the oracle's for the microbatch [t0, t0 + n): slots, counts, layout
+    ranges and every packed message (codes, scales, source)."""
+    n = T - t0 if n is None else n
+    L = E // R
+    eq(pk["slot"][:, t0:t0 + n], sent["slot"][:, t0:t0 + n], "slot")
+    eq(pk["packed_recv_count"], o_pk["packed_recv_count"], "packed_recv_count")
+    eq(pk["layout_range"], o_pk["layout_range"], "layout_range")
+    px, ps, pi = bits(pk["packed_x"]), bits(pk["packed_scales"]), bits(pk["packed_src_info"])
+    for d in range(R):
+        for l in range(L):
+            c = int(o_pk["packed_recv_count"][d, l])
+            eq(px[d, l, :c], o_pk["packed_x"][d, l, :c], f"packed_x[{d},{l}]")
+            eq(ps[d, l, :c], o_pk["packed_scales"][d, l, :c], f"packed_scales[{d},{l}]")
+            eq(pi[d, l, :c], o_pk["packed_src_info"][d, l, :c], f"packed_src_info[{d},{l}]")

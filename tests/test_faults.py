@@ -196,3 +196,32 @@ def test_expert_alignment_limits():
     assert e.value.status == "EP_ERR_INVALID_ARG"
     assert big.expert_alignment == 1024
     big.close()
+
+
+def test_ll_invalid_topk_is_reported_and_the_rest_exact():
+    """An expert index outside [-1, E) in the low-latency send is skipped and
+    flagged (EP_ERR_INVALID_INPUT at the next check); every other entry's
+    slot, count and packed message equals the oracle's on the same routing
+    with those entries masked."""
+    import oracle as orc
+    from parity_util import check_ll_microbatch_equal
+    R, E, K, T, H, cap = 4, 16, 4, 10, 256, 10
+    idx = inputs.random_topk(R, E, K, T, 17, 0.1)
+    x = inputs.random_x(R, T, H, 17)
+    bad = idx.clone()
+    bad[1, 3, 2] = E
+    bad[3, 9, 0] = -3
+    masked = bad.clone()
+    masked[1, 3, 2] = -1
+    masked[3, 9, 0] = -1
+    buf = LLBuffer(R, E, K, T, H, cap)
+    pk = buf.dispatch(x.cuda(), bad.cuda())
+    torch.cuda.synchronize()
+    with pytest.raises(EpError) as e:
+        buf.check()
+    assert e.value.status == "EP_ERR_INVALID_INPUT"
+    buf.check()  # cleared
+    sent = orc.ll_send(x, masked, R, E, cap)
+    o_pk = orc.ll_pack(sent, R, E, H, cap)
+    check_ll_microbatch_equal(pk, sent, o_pk, R, E, T, cap)
+    assert int(pk["packed_recv_count"].sum()) == int((masked >= 0).sum())
