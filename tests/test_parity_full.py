@@ -287,3 +287,106 @@ def test_prefill_full_fp8_one_pass():
     _rows_equal(recv["recv_xq"][:, :n_def], q, recv_tok, "recv_xq (one pass)")
     for k in ("recv_src_rank", "recv_src_idx", "recv_topk_idx", "recv_topk_weights"):
         eq(recv[k], o_disp[k], k)
+
+
+def _combine_sampled(out, xf, idx, w, R, E, K, T, H, what):
+    """Identity-expert combine of sampled tokens against the oracle's
+    sub-problem (every entry of a token reads the token's own row)."""
+    rng = np.random.default_rng(13)
+    g = rng.choice(R * T, size=min(N_SAMPLES, R * T), replace=False)
+    gd = torch.from_numpy(g).cuda()
+    xs = bits(xf.index_select(0, gd))
+    exp = _combine_sub_problem(np.repeat(xs[:, None, :], K, axis=1), idx.numpy().reshape(R * T, K),
+                               w.numpy().reshape(R * T, K), g, R, E, K, False, 1)
+    eq(bits(out.view(R * T, H).index_select(0, gd)), exp, what)
+
+
+def test_prefill_full_expert_aligned():
+    """The permute into 128-row aligned expert blocks at the prefill size (the
+    bench's expert_aligned leg): the handle's offsets, every pair's position and
+    row, and the combine reading the aligned layout."""
+    wl = inputs.WORKLOADS["prefill"]
+    R, E, K, T, H, C = wl.R, wl.E, wl.K, wl.T, wl.H, wl.num_channels
+    align = 128
+    idx, w = inputs.make_routing(wl, 0)
+    x = inputs.make_x(wl, 0, device="cuda")
+    xf = x.view(R * T, H)
+    ctx = Context(R, E, K, T, H, num_channels=C, expert_alignment=align)
+    idxd, wd = idx.cuda(), w.cuda()
+    h = ctx.notify_dispatch(idxd, ctx.get_dispatch_layout(idxd))
+    recv = ctx.dispatch(x, idxd, wd, h)
+    perm = ctx.permute(h, recv)
+    out = ctx.combine(h, perm["permuted_x"], idxd, wd)
+    ctx.check()
+    torch.cuda.synchronize()
+    o_note = orc.notify(orc.layout(idx, R, E), R, E, T, C, align=align)
+    for k in ("num_recv_per_expert", "expert_offsets", "perm_rank_base"):
+        eq(h[k], o_note[k], k)
+    o_disp = orc.dispatch(np.zeros((R, T, 8), np.uint16), idx, w, o_note, R, E)
+    o_perm = orc.permute(idx, o_disp["recv_x"], o_note, R, E)
+    eq(h["perm_pos"], o_perm["perm_pos"], "perm_pos")
+    psr = o_perm["perm_src_row"]
+    used = np.nonzero(psr >= 0)[0]
+    assert perm["permuted_x"].shape[0] == len(psr)
+    eq(perm["perm_src_row"].cpu().numpy()[used], psr[used], "perm_src_row (pairs' rows)")
+    src_tok = o_disp["recv_src_rank"].astype(np.int64) * T + o_disp["recv_src_idx"]
+    _rows_equal(perm["permuted_x"], xf, src_tok[psr[used]], "permuted_x (aligned)", got_rows=used)
+    _combine_sampled(out, xf, idx, w, R, E, K, T, H, "combine of the aligned layout (sampled tokens)")
+
+
+def test_prefill_full_no_wait_graph():
+    """The prefill step without the host wait, captured in one CUDA graph and
+    replayed (the bench's graph leg): worst-case buffers, row totals read on
+    the device; the handle, every received and permuted row, and sampled
+    combine tokens equal the oracle's."""
+    wl = inputs.WORKLOADS["prefill"]
+    R, E, K, T, H, C = wl.R, wl.E, wl.K, wl.T, wl.H, wl.num_channels
+    idx, w = inputs.make_routing(wl, 0)
+    x = inputs.make_x(wl, 0, device="cuda")
+    xf = x.view(R * T, H)
+    ctx = Context(R, E, K, T, H, num_channels=C)
+    idxd, wd = idx.cuda(), w.cuda()
+    rmax, pmax, _ = ctx.max_rows
+    recv = ctx.alloc_recv(rmax)
+    perm = dict(permuted_x=torch.empty(pmax, H, dtype=torch.bfloat16, device="cuda"),
+                perm_src_row=torch.empty(pmax, dtype=torch.int32, device="cuda"))
+    out = torch.empty(R, T, H, dtype=torch.bfloat16, device="cuda")
+    lay = {k: v for k, v in ctx.get_dispatch_layout(idxd).items()}
+    h = ctx.alloc_handle()
+
+    def step():
+        ctx.get_dispatch_layout(idxd, out=lay)
+        ctx.notify_dispatch(idxd, lay, handle=h, wait=False)
+        ctx.dispatch(x, idxd, wd, h, out=recv)
+        ctx.permute(h, recv, out=perm)
+        ctx.combine(h, perm["permuted_x"], idxd, wd, out=out)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()  # once outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    recv["recv_x"].zero_()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    g.replay()
+    torch.cuda.synchronize()
+    ctx.check()
+    o_note = orc.notify(orc.layout(idx, R, E), R, E, T, C)
+    for k in ("recv_count", "num_recv_tokens", "recv_offsets", "rank_base", "num_recv_per_expert",
+              "expert_offsets", "perm_rank_base", "channel_prefix_matrix", "send_pos"):
+        eq(h[k], o_note[k], k)
+    nr, npm = int(o_note["rank_base"][R]), int(o_note["perm_rank_base"][R])
+    o_disp = orc.dispatch(np.zeros((R, T, 8), np.uint16), idx, w, o_note, R, E)
+    for k in ("recv_src_rank", "recv_src_idx", "recv_topk_idx", "recv_topk_weights"):
+        eq(recv[k][:nr], o_disp[k], k)
+    o_perm = orc.permute(idx, o_disp["recv_x"], o_note, R, E)
+    eq(h["perm_pos"], o_perm["perm_pos"], "perm_pos")
+    eq(perm["perm_src_row"][:npm], o_perm["perm_src_row"], "perm_src_row")
+    src_tok = o_disp["recv_src_rank"].astype(np.int64) * T + o_disp["recv_src_idx"]
+    _rows_equal(recv["recv_x"][:nr], xf, src_tok, "recv_x (graph replay)")
+    _rows_equal(perm["permuted_x"][:npm], xf, src_tok[o_perm["perm_src_row"]], "permuted_x (graph replay)")
+    _combine_sampled(out, xf, idx, w, R, E, K, T, H, "combine (graph replay, sampled tokens)")
