@@ -158,6 +158,75 @@ def test_hier_full_staged():
     _normal_full(inputs.WORKLOADS["hier"], hier=True)
 
 
+def _identity_y(pk, R):
+    """The identity expert on the packed messages: y = bf16(code * scale)."""
+    y = torch.empty(pk["packed_x"].shape, dtype=torch.bfloat16, device="cuda")
+    for d in range(R):
+        y[d] = (pk["packed_x"][d].view(torch.float8_e4m3fn).float() *
+                pk["packed_scales"][d].repeat_interleave(128, dim=-1)).to(torch.bfloat16)
+    return y
+
+
+def _check_ll_microbatch_full(pk, outs, xf, q, idx, w, R, E, K, T, H, cap, t0, n, rng, what=""):
+    """Every message of the microbatch against the oracle's quantisation of its
+    source token (codes, scales, source), the slots and the receive layout
+    exactly, and sampled tokens of each combine output against the oracle's
+    k-ordered sum.  outs: [(out, y, y_is_identity)]."""
+    L = E // R
+    idx_np, w_np = idx.numpy(), w.numpy()
+    # integers exactly (slots do not depend on H: the oracle runs on a 128-channel stand-in)
+    sent = orc.ll_send(np.zeros((R, T, 128), np.uint16), idx, R, E, cap, t0, n)
+    o_pk = orc.ll_pack(sent, R, E, 128, cap)
+    eq(pk["slot"][:, t0:t0 + n], sent["slot"][:, t0:t0 + n], "slot" + what)
+    eq(pk["packed_recv_count"], o_pk["packed_recv_count"], "packed_recv_count" + what)
+    eq(pk["layout_range"], o_pk["layout_range"], "layout_range" + what)
+    # every message of the microbatch: codes, scales and source of each valid (s, t, k)
+    s_, t_, k_ = np.nonzero(idx_np[:, t0:t0 + n] >= 0)
+    t_ = t_ + t0
+    e_ = idx_np[s_, t_, k_]
+    d_, l_ = e_ // L, e_ % L
+    lr = o_pk["layout_range"]
+    row = lr[d_, l_, s_, 0] + sent["slot"][s_, t_, k_]
+    msg = (d_ * L + l_) * (R * cap) + row
+    tok = s_ * T + t_
+    _rows_equal(pk["packed_x"].view(-1, H), q[:, :H], tok, "packed_x (every message)" + what, got_rows=msg)
+    _rows_equal(pk["packed_scales"].view(-1, H // 128), q[:, H:].view(torch.float32), tok,
+                "packed_scales (every message)" + what, got_rows=msg)
+    src_info = torch.from_numpy(np.stack([s_, t_], axis=1).astype(np.int32)).cuda()
+    _rows_equal(pk["packed_src_info"].view(-1, 2), src_info, np.arange(len(msg)),
+                "packed_src_info (every message)" + what, got_rows=msg)
+    # sampled tokens of the microbatch: the oracle's k-ordered fp32 sum on a
+    # one-rank sub-problem (one expert per k, one slot per token)
+    toks = rng.choice(R * n, size=min(128, R * n), replace=False)
+    gs = [(int(qq // n), int(t0 + qq % n)) for qq in toks]
+    m = len(gs)
+    sub_idx = np.full((1, m, K), -1, np.int64)
+    sub_w = np.zeros((1, m, K), np.float32)
+    sub_slot = np.full((1, m, K), -1, np.int32)
+    sub_lr = np.zeros((1, K, 1, 2), np.int32)
+    sub_lr[..., 1] = m
+    for out, y, identity in outs:
+        y_sub = np.zeros((1, K, m, H), np.uint16)
+        yf = y.view(-1, H)
+        for i, (s, t) in enumerate(gs):
+            if identity:
+                codes, scales = orc.quantize_row(bits(xf[s * T + t]))
+                yrow = orc.ll_dequant(codes[None], scales[None])[0]
+            for k in range(K):
+                e = int(idx_np[s, t, k])
+                if e >= 0:
+                    sub_idx[0, i, k] = k
+                    sub_w[0, i, k] = w_np[s, t, k]
+                    sub_slot[0, i, k] = i
+                    d, l = divmod(e, L)
+                    y_sub[0, k, i] = yrow if identity else \
+                        bits(yf[(d * L + l) * R * cap + lr[d, l, s, 0] + sent["slot"][s, t, k]])
+        exp = orc.ll_combine(y_sub, sub_idx, sub_w, sub_slot, sub_lr, 1, K, m)[0]
+        got = np.stack([bits(out[s, t]) for s, t in gs])
+        kind = "identity expert" if identity else "distinct expert rows"
+        eq(got, exp, f"ll combine of the {kind} (sampled tokens, microbatch {t0}){what}")
+
+
 def _ll_full(wl):
     R, E, K, T, H, cap = wl.R, wl.E, wl.K, wl.T, wl.H, wl.ll_cap
     L = E // R
@@ -169,75 +238,20 @@ def _ll_full(wl):
     out = torch.zeros(R, T, H, dtype=torch.bfloat16, device="cuda")
     out_y = torch.zeros(R, T, H, dtype=torch.bfloat16, device="cuda")
     pk = buf.alloc_packed()
-    y_ll = torch.empty(pk["packed_x"].shape, dtype=torch.bfloat16, device="cuda")
-    y_rand = inputs.random_rows(R * L * R * cap, H, seed=77, device="cuda").view(y_ll.shape)
+    y_rand = inputs.random_rows(R * L * R * cap, H, seed=77, device="cuda").view(pk["packed_x"].shape)
     q = _oracle_fp8_rows(xf)                    # every token's codes and scales, by the oracle
-    probe = np.zeros((R, T, 128), np.uint16)
     rng = np.random.default_rng(11)
-    idx_np, w_np = idx.numpy(), w.numpy()
     for t0 in range(0, T, cap):
         n = min(cap, T - t0)
         buf.dispatch(x, idxd, t0, n, out=pk)
         buf.check()
-        # identity expert (the expert is not part of the path): y = bf16(code * scale)
-        for d in range(R):
-            y_ll[d] = (pk["packed_x"][d].view(torch.float8_e4m3fn).float() *
-                       pk["packed_scales"][d].repeat_interleave(128, dim=-1)).to(torch.bfloat16)
+        y_ll = _identity_y(pk, R)
         buf.combine(y_ll, idxd, wd, pk, t0, n, out=out)
         buf.combine(y_rand, idxd, wd, pk, t0, n, out=out_y)
         buf.check()
-        # integers exactly (slots do not depend on H: the oracle runs on a 128-channel stand-in)
-        sent = orc.ll_send(probe, idx, R, E, cap, t0, n)
-        o_pk = orc.ll_pack(sent, R, E, 128, cap)
-        eq(pk["slot"][:, t0:t0 + n], sent["slot"][:, t0:t0 + n], "slot")
-        eq(pk["packed_recv_count"], o_pk["packed_recv_count"], "packed_recv_count")
-        eq(pk["layout_range"], o_pk["layout_range"], "layout_range")
-        # every message of the microbatch: codes, scales and source of each valid (s, t, k)
-        s_, t_, k_ = np.nonzero(idx_np[:, t0:t0 + n] >= 0)
-        t_ = t_ + t0
-        e_ = idx_np[s_, t_, k_]
-        d_, l_ = e_ // L, e_ % L
-        lr = o_pk["layout_range"]
-        row = lr[d_, l_, s_, 0] + sent["slot"][s_, t_, k_]
-        msg = (d_ * L + l_) * (R * cap) + row
-        tok = s_ * T + t_
-        _rows_equal(pk["packed_x"].view(-1, H), q[:, :H], tok, "packed_x (every message)", got_rows=msg)
-        _rows_equal(pk["packed_scales"].view(-1, H // 128), q[:, H:].view(torch.float32), tok,
-                    "packed_scales (every message)", got_rows=msg)
-        src_info = torch.from_numpy(np.stack([s_, t_], axis=1).astype(np.int32)).cuda()
-        _rows_equal(pk["packed_src_info"].view(-1, 2), src_info, np.arange(len(msg)),
-                    "packed_src_info (every message)", got_rows=msg)
-        # sampled tokens of the microbatch: the oracle's k-ordered fp32 sum on a
-        # one-rank sub-problem (one expert per k, one slot per token)
-        toks = rng.choice(R * n, size=min(128, R * n), replace=False)
-        gs = [(int(qq // n), int(t0 + qq % n)) for qq in toks]
-        m = len(gs)
-        sub_idx = np.full((1, m, K), -1, np.int64)
-        sub_w = np.zeros((1, m, K), np.float32)
-        sub_slot = np.full((1, m, K), -1, np.int32)
-        y_sub = np.zeros((1, K, m, H), np.uint16)
-        y_sub_r = np.zeros((1, K, m, H), np.uint16)
-        yr_flat = y_rand.view(-1, H)
-        for i, (s, t) in enumerate(gs):
-            codes, scales = orc.quantize_row(bits(xf[s * T + t]))
-            yrow = orc.ll_dequant(codes[None], scales[None])[0]
-            for k in range(K):
-                e = int(idx_np[s, t, k])
-                if e >= 0:
-                    sub_idx[0, i, k] = k
-                    sub_w[0, i, k] = w_np[s, t, k]
-                    sub_slot[0, i, k] = i
-                    y_sub[0, k, i] = yrow
-                    d, l = divmod(e, L)
-                    y_sub_r[0, k, i] = bits(yr_flat[(d * L + l) * R * cap + lr[d, l, s, 0] + sent["slot"][s, t, k]])
-        sub_lr = np.zeros((1, K, 1, 2), np.int32)
-        sub_lr[..., 1] = m
-        exp = orc.ll_combine(y_sub, sub_idx, sub_w, sub_slot, sub_lr, 1, K, m)[0]
-        got = np.stack([bits(out[s, t]) for s, t in gs])
-        eq(got, exp, f"ll combine (sampled tokens, microbatch {t0})")
-        exp = orc.ll_combine(y_sub_r, sub_idx, sub_w, sub_slot, sub_lr, 1, K, m)[0]
-        got = np.stack([bits(out_y[s, t]) for s, t in gs])
-        eq(got, exp, f"ll combine of distinct expert rows (sampled tokens, microbatch {t0})")
+        _check_ll_microbatch_full(pk, [(out, y_ll, True), (out_y, y_rand, False)], xf, q, idx, w, R, E, K, T, H,
+                                  cap, t0, n, rng)
+        del y_ll
 
 
 def test_decode_ll_full():
@@ -390,3 +404,61 @@ def test_prefill_full_no_wait_graph():
     _rows_equal(recv["recv_x"][:nr], xf, src_tok, "recv_x (graph replay)")
     _rows_equal(perm["permuted_x"][:npm], xf, src_tok[o_perm["perm_src_row"]], "permuted_x (graph replay)")
     _combine_sampled(out, xf, idx, w, R, E, K, T, H, "combine (graph replay, sampled tokens)")
+
+
+def test_decode_ll_full_graph_and_two_streams():
+    """The decode layer as the bench also times it: replayed from a CUDA graph,
+    and two microbatches (two buffers, different tokens) sent, received and
+    combined on two streams at once.  Every message and sampled combine
+    tokens of each equal the oracle's."""
+    wl = inputs.WORKLOADS["decode"]
+    R, E, K, T, H, cap = wl.R, wl.E, wl.K, wl.T, wl.H, wl.ll_cap
+    L = E // R
+    rng = np.random.default_rng(19)
+    lanes = []
+    for seed in (0, 1):
+        idx, w = inputs.make_routing(wl, seed)
+        x = inputs.make_x(wl, seed, device="cuda")
+        buf = LLBuffer(R, E, K, T, H, cap)
+        pk = buf.alloc_packed()
+        y = inputs.random_rows(R * L * R * cap, H, seed=31 + seed, device="cuda").view(pk["packed_x"].shape)
+        out = torch.zeros(R, T, H, dtype=torch.bfloat16, device="cuda")
+        lanes.append(dict(idx=idx, w=w, x=x, idxd=idx.cuda(), wd=w.cuda(), buf=buf, pk=pk, y=y, out=out,
+                          q=_oracle_fp8_rows(x.view(R * T, H))))
+    # one lane as a CUDA graph, replayed
+    a = lanes[0]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        a["buf"].dispatch(a["x"], a["idxd"], out=a["pk"])
+        a["buf"].combine(a["y"], a["idxd"], a["wd"], a["pk"], out=a["out"])
+    side.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        a["buf"].dispatch(a["x"], a["idxd"], out=a["pk"])
+        a["buf"].combine(a["y"], a["idxd"], a["wd"], a["pk"], out=a["out"])
+    a["out"].zero_()
+    a["pk"]["packed_recv_count"].fill_(-5)
+    g.replay()
+    torch.cuda.synchronize()
+    a["buf"].check()
+    _check_ll_microbatch_full(a["pk"], [(a["out"], a["y"], False)], a["x"].view(R * T, H), a["q"], a["idx"], a["w"],
+                              R, E, K, T, H, cap, 0, T, rng, " (graph replay)")
+    del g
+    # both lanes on two streams at once
+    streams = (torch.cuda.Stream(), torch.cuda.Stream())
+    main = torch.cuda.current_stream()
+    for ln in lanes:
+        ln["out"].zero_()
+    for st, ln in zip(streams, lanes):
+        st.wait_stream(main)
+        with torch.cuda.stream(st):
+            ln["buf"].dispatch(ln["x"], ln["idxd"], out=ln["pk"])
+            ln["buf"].combine(ln["y"], ln["idxd"], ln["wd"], ln["pk"], out=ln["out"])
+    for st in streams:
+        main.wait_stream(st)
+    torch.cuda.synchronize()
+    for i, ln in enumerate(lanes):
+        ln["buf"].check()
+        _check_ll_microbatch_full(ln["pk"], [(ln["out"], ln["y"], False)], ln["x"].view(R * T, H), ln["q"], ln["idx"],
+                                  ln["w"], R, E, K, T, H, cap, 0, T, rng, f" (stream {i} of two)")
