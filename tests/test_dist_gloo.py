@@ -1,5 +1,5 @@
-"""The N>1 bookkeeping of the benchmark on CPU: two gloo ranks, each with its
-own seeded batch, run the oracle's path independently (no data crosses ranks)
+"""The N>1 bookkeeping of the benchmark on CPU: two and four gloo ranks, each
+with its own seeded batch, run the oracle's path independently (no data crosses ranks)
 and agree on the max step time and the summed token count."""
 import os
 import socket
@@ -36,8 +36,8 @@ def _worker(rank, world, port, q):
     epdist.shutdown()
 
 
-def test_two_gloo_ranks_weak_scaling():
-    world = 2
+@pytest.mark.parametrize("world", [2, 4])
+def test_gloo_ranks_weak_scaling(world):
     port = _free_port()
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
@@ -49,12 +49,11 @@ def test_two_gloo_ranks_weak_scaling():
         p.join(timeout=60)
         assert p.exitcode == 0
     got.sort()
-    (r0, w0, s0, m0, t0, n0, o0), (r1, w1, s1, m1, t1, n1, o1) = got
-    assert (r0, r1) == (0, 1) and w0 == w1 == 2
-    assert s0 != s1                      # independent batches
-    assert m0 == m1 == 2.0               # max over ranks
-    assert t0 == t1 == 2 * 4 * 16        # whole-job tokens
-    assert o0 != o1                      # each rank combined its own tokens
+    assert [g[0] for g in got] == list(range(world)) and all(g[1] == world for g in got)
+    assert len({g[2] for g in got}) == world            # independent batches
+    assert all(g[3] == float(world) for g in got)       # max over ranks of the stand-in times 1..world
+    assert all(g[4] == world * 4 * 16 for g in got)     # whole-job tokens
+    assert len({g[6] for g in got}) == world            # each rank combined its own tokens
 
 
 def test_single_process_defaults(monkeypatch):
