@@ -845,7 +845,6 @@ def main():
         torch.cuda.synchronize()
         buf.check()
         lname = ["ll_send", "ll_recv", "ll_combine"]
-        lper = {n: statistics.median(e[j].elapsed_time(e[j + 1]) for e in lev) for j, n in enumerate(lname)}
         # each kernel alone: L2 flushed (and its dirty lines written back)
         # right before it, so that no kernel pays for the previous one's
         # write-backs nor gains from its lines still in L2
@@ -1020,9 +1019,8 @@ def main():
               "us_per_layer_cuda_graph": graph_us,
               "dual_microbatch_overlap": dual,
               "signal_wait": waits, "slot_utilisation": slot_util,
-              "kernels": {n: {"us": round(lper[n] * 1e3, 2), "algo_bytes": lbytes[n],
-                              "GBps": round(lbytes[n] / (lper[n] * 1e-3) / 1e9, 1),
-                              "frac": round(lbytes[n] / (lper[n] * 1e-3) / 1e9 / peak, 3)} for n in lname},
+              "kernels": {n: kernel_entry([e[j].elapsed_time(e[j + 1]) for e in lev], lbytes[n], peak)
+                          for j, n in enumerate(lname)},
               "kernels_isolated": {n: kernel_entry(iso[n], lbytes[n], peak) for n in lname},
               "kernels_isolated_how": "each kernel with L2 flushed and written back right before it "
                                       "(the chained figures above are the layer's own)",
